@@ -1,0 +1,210 @@
+"""Python binding of libqerl, the sm_103a NVFP4 weight-only LoRA linear library.
+
+Argument marshalling only: each function passes torch tensors' device pointers,
+sizes and the current CUDA stream to the C entry point of the same name in
+``include/qerl.h`` and raises ``QerlError`` on a non-OK status.  Every step of
+the computation runs in the library's CUDA kernels; there is no fallback.  If
+``_lib/libqerl.so`` is missing the import of the library fails loudly (run
+``build()``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libqerl.so")
+
+QERL_OK = 0
+STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARG", 2: "QERL_ERR_SHAPE", 3: "QERL_ERR_ALIGN",
+                4: "QERL_ERR_NONFINITE", 5: "QERL_ERR_CUDA", 6: "QERL_ERR_TIMEOUT",
+                7: "QERL_ERR_UNSUPPORTED_DEVICE", 8: "QERL_ERR_WORKSPACE"}
+SCALE_ROUND_UP, SCALE_ROUND_NEAREST_EVEN = 0, 1
+OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_AQN_RMSNORM = 0, 1, 2, 3
+ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
+
+# Every C symbol include/qerl.h declares (checked by the CPU test suite).
+EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_linear_fwd",
+            "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_noise", "qerl_aqn_sigma",
+            "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
+            "qerl_launch_count"]
+
+
+class QerlError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class _QuantOpts(C.Structure):
+    _fields_ = [("scale_round", C.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)
+
+
+def lib() -> C.CDLL:
+    """The loaded libqerl.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"libqerl.so not built ({LIB_PATH}); call "
+                                  "nvfp4_weight_only_quantize_gb300.build()")
+            L = C.CDLL(LIB_PATH)
+            vp, i64, i32, f32, u64, u32, sz = (C.c_void_p, C.c_int64, C.c_int, C.c_float, C.c_uint64,
+                                               C.c_uint32, C.c_size_t)
+            sig = {
+                "qerl_nvfp4_quantize": ([vp, i64, i64, i64, vp, vp, vp, vp, vp, sz, vp], i32),
+                "qerl_nvfp4_dequantize": ([vp, vp, vp, i64, i64, vp, i32, vp], i32),
+                "qerl_nvfp4_lora_linear_fwd": ([vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp, vp,
+                                                sz, vp], i32),
+                "qerl_nvfp4_lora_linear_bwd": ([vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp,
+                                                vp, vp, i32, vp, sz, vp], i32),
+                "qerl_aqn_rmsnorm": ([vp, i64, i64, vp, f32, f32, u64, u64, u32, vp, vp, sz, vp], i32),
+                "qerl_aqn_noise": ([i64, u64, u64, u32, vp, vp, vp], i32),
+                "qerl_aqn_sigma": ([i64, i64, f32, f32, i32], f32),
+                "qerl_workspace_bytes": ([i32, i64, i64, i64, i32], sz),
+                "qerl_get_error": ([vp], i32),
+                "qerl_status_string": ([i32], C.c_char_p),
+                "qerl_set_linear_algo": ([i32], i32),
+                "qerl_launch_count": ([], u64),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().qerl_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != QERL_OK:
+        raise QerlError(status, where)
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int, r: int) -> int:
+    return lib().qerl_workspace_bytes(op, M, N, K, r)
+
+
+def workspace(op: int, M: int, N: int, K: int, r: int, device="cuda") -> torch.Tensor:
+    """A caller-owned scratch buffer of the size the library asks for."""
+    return torch.empty(max(workspace_bytes(op, M, N, K, r), 1), dtype=torch.uint8, device=device)
+
+
+def set_linear_algo(algo: int):
+    _check(lib().qerl_set_linear_algo(algo), "qerl_set_linear_algo")
+
+
+def launch_count() -> int:
+    return lib().qerl_launch_count()
+
+
+def get_error(stream=None) -> int:
+    return lib().qerl_get_error(_stream(stream))
+
+
+# ---------------------------------------------------------------- quantizer
+def qerl_nvfp4_quantize(W: torch.Tensor, scale_round: int = SCALE_ROUND_UP, out=None, ws=None, stream=None):
+    """W bf16 [N, K] (row stride W.stride(0)) -> (codes u8 [N,K/2], scales u8 [N,K/16], s_t f32 [1])."""
+    assert W.dtype == torch.bfloat16 and W.dim() == 2 and W.stride(1) == 1
+    N, K = W.shape
+    if out is None:
+        out = (torch.empty(N, K // 2, dtype=torch.uint8, device=W.device),
+               torch.empty(N, K // 16, dtype=torch.uint8, device=W.device),
+               torch.empty(1, dtype=torch.float32, device=W.device))
+    codes, scales, ts = out
+    ws = workspace(OP_QUANTIZE, 0, N, K, 0, W.device) if ws is None else ws
+    opts = _QuantOpts(scale_round)
+    _check(lib().qerl_nvfp4_quantize(_p(W), N, K, W.stride(0), _p(codes), _p(scales), _p(ts), C.byref(opts),
+                                     _p(ws), ws.numel(), _stream(stream)), "qerl_nvfp4_quantize")
+    return codes, scales, ts
+
+
+def qerl_nvfp4_dequantize(codes, scales, tensor_scale, N: int, K: int, apply_tensor_scale: bool = True,
+                          out=None, stream=None):
+    out = torch.empty(N, K, dtype=torch.bfloat16, device=codes.device) if out is None else out
+    _check(lib().qerl_nvfp4_dequantize(_p(codes), _p(scales), _p(tensor_scale), N, K, _p(out),
+                                       int(apply_tensor_scale), _stream(stream)), "qerl_nvfp4_dequantize")
+    return out
+
+
+# ---------------------------------------------------------------- linear
+def qerl_nvfp4_lora_linear_fwd(x, codes, scales, tensor_scale, A, B, lora_scale: float, y=None, t_out=None,
+                               ws=None, stream=None):
+    """y = x w_hat^T + s (x A^T) B^T.  x bf16 [M,K], A bf16 [r,K], B bf16 [N,r] -> y bf16 [M,N]."""
+    M, K = x.shape
+    N, r = B.shape
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
+    ws = workspace(OP_LINEAR_FWD, M, N, K, r, x.device) if ws is None else ws
+    _check(lib().qerl_nvfp4_lora_linear_fwd(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A), _p(B),
+                                            r, float(lora_scale), _p(y), _p(t_out), _p(ws), ws.numel(),
+                                            _stream(stream)), "qerl_nvfp4_lora_linear_fwd")
+    return y
+
+
+def qerl_nvfp4_lora_linear_bwd(dy, x, codes, scales, tensor_scale, A, B, lora_scale: float, t_saved=None,
+                               dx=None, dA=None, dB=None, accumulate: bool = False, want=("dx", "dA", "dB"),
+                               ws=None, stream=None):
+    """Returns (dx bf16 [M,K], dA f32 [r,K], dB f32 [N,r]); outputs not in ``want`` are None."""
+    M, N = dy.shape
+    K = x.shape[1]
+    r = A.shape[0]
+    dev = x.device
+    if dx is None and "dx" in want:
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    if dA is None and "dA" in want:
+        dA = torch.zeros(r, K, dtype=torch.float32, device=dev)
+    if dB is None and "dB" in want:
+        dB = torch.zeros(N, r, dtype=torch.float32, device=dev)
+    ws = workspace(OP_LINEAR_BWD, M, N, K, r, dev) if ws is None else ws
+    _check(lib().qerl_nvfp4_lora_linear_bwd(_p(dy), _p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A),
+                                            _p(B), r, float(lora_scale), _p(t_saved), _p(dx), _p(dA), _p(dB),
+                                            int(accumulate), _p(ws), ws.numel(), _stream(stream)),
+           "qerl_nvfp4_lora_linear_bwd")
+    return dx, dA, dB
+
+
+# ---------------------------------------------------------------- AQN
+def qerl_aqn_rmsnorm(x, gamma, eps: float, sigma: float, seed: int, step: int, layer_id: int, y=None, ws=None,
+                     stream=None):
+    M, H = x.shape
+    y = torch.empty_like(x) if y is None else y
+    ws = workspace(OP_AQN_RMSNORM, M, 0, H, 0, x.device) if ws is None else ws
+    _check(lib().qerl_aqn_rmsnorm(_p(x), M, H, _p(gamma), float(eps), float(sigma), seed, step, layer_id, _p(y),
+                                  _p(ws), ws.numel(), _stream(stream)), "qerl_aqn_rmsnorm")
+    return y
+
+
+def qerl_aqn_noise(H: int, seed: int, step: int, layer_id: int, want_raw: bool = False, device="cuda",
+                   stream=None):
+    z = torch.empty(H, dtype=torch.float32, device=device)
+    raw = torch.empty(H, dtype=torch.int64, device=device) if want_raw else None
+    _check(lib().qerl_aqn_noise(H, seed, step, layer_id, _p(z), _p(raw), _stream(stream)), "qerl_aqn_noise")
+    return (z, raw) if want_raw else z
+
+
+def qerl_aqn_sigma(step: int, total_steps: int, sigma_start: float, sigma_end: float, num_stages: int) -> float:
+    return lib().qerl_aqn_sigma(step, total_steps, sigma_start, sigma_end, num_stages)
