@@ -1,0 +1,360 @@
+"""Benchmark of the NVFP4 weight-only LoRA decode layer (Qwen2.5-7B shapes).
+
+One step = one decoder layer of rollout decode through the library:
+  AQN-RMSNorm(h) -> q_proj, k_proj, v_proj -> o_proj(attention stand-in)
+  -> AQN-RMSNorm -> gate_proj, up_proj -> down_proj(up output),
+M = 64 tokens, LoRA r = 32 on every linear.  Attention and SwiGLU are not part of
+the path; o_proj takes a random bf16 stand-in for the attention output and
+down_proj takes up_proj's output.  Weights rotate over several layer copies
+whose NVFP4 bytes exceed L2, so every step streams its weights from HBM.
+
+Metric: HBM GB/s of algorithmic bytes, N*K*0.5625 + 4 + 2*r*(N+K) per linear
+(NVFP4 weight + tensor scale + bf16 LoRA), activations excluded.
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def linear_bytes(N, K, r):
+    return N * K * 0.5625 + 4 + 2 * r * (N + K)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ ranks
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def combine_ranks(local_seconds: float, local_units: float):
+    """(max time over ranks, total units over ranks); replicas run independently."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_seconds, local_units
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([s.strip() for s in line.split(",")])
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        sms = [float(r[0]) for r in self.rows if len(r) >= 7 and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if len(r) >= 7 and r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) >= 7:
+                for n, v in zip(names, r[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ our arm
+class DecodeLayer:
+    """NVFP4 weights + LoRA adapters + norm scales of n_copies Qwen2.5-7B layers."""
+
+    def __init__(self, wl, n_copies, device):
+        import nvfp4_weight_only_quantize_gb300 as q
+        from nvfp4_weight_only_quantize_gb300 import synth
+        self.q, self.wl, self.copies = q, wl, []
+        for c in range(n_copies):
+            lins = []
+            for i, (name, N, K) in enumerate(wl.linears):
+                base = synth.seed_of(1, c, 16 * i)
+                W = synth.weight(N, K, base + synth.T_W, device)
+                codes, scales, ts = q.qerl_nvfp4_quantize(W)
+                del W
+                A = synth.lora_A(wl.r, K, base + synth.T_A, device)
+                B = synth.lora_B(N, wl.r, base + synth.T_B, device)
+                lins.append((name, N, K, codes, scales, ts, A, B))
+            gammas = [synth.norm_gamma(wl.hidden, synth.seed_of(1, c, 200 + j), device) for j in range(2)]
+            self.copies.append((lins, gammas))
+        torch.cuda.synchronize()
+        self.bytes_per_step = sum(linear_bytes(N, K, wl.r) for _, N, K in wl.linears)
+
+    def buffers(self, M, device):
+        wl = self.wl
+        outs = {name: torch.empty(M, N, dtype=torch.bfloat16, device=device) for name, N, K in wl.linears}
+        ws_lin = max(self.q.workspace_bytes(self.q.OP_LINEAR_FWD, M, N, K, wl.r) for _, N, K in wl.linears)
+        return dict(outs=outs, h1=torch.empty(M, wl.hidden, dtype=torch.bfloat16, device=device),
+                    h2=torch.empty(M, wl.hidden, dtype=torch.bfloat16, device=device),
+                    ws=torch.empty(max(ws_lin, 1), dtype=torch.uint8, device=device),
+                    ws_norm=self.q.workspace(self.q.OP_AQN_RMSNORM, M, 0, wl.hidden, 0, device))
+
+    def step(self, copy, x, attn, buf, sigma, step_idx, ev=None):
+        """One decoder layer; ev: optional dict name -> list of (start, end) events."""
+        q = self.q
+        lins, gammas = self.copies[copy]
+        o = buf["outs"]
+        q.qerl_aqn_rmsnorm(x, gammas[0], 1e-6, sigma, 1, step_idx, 2 * copy, y=buf["h1"], ws=buf["ws_norm"])
+        src = {"q_proj": buf["h1"], "k_proj": buf["h1"], "v_proj": buf["h1"], "o_proj": attn}
+        for name, N, K, codes, scales, ts, A, B in lins:
+            if name == "gate_proj":
+                q.qerl_aqn_rmsnorm(o["o_proj"], gammas[1], 1e-6, sigma, 1, step_idx, 2 * copy + 1, y=buf["h2"],
+                                   ws=buf["ws_norm"])
+                src["gate_proj"] = src["up_proj"] = buf["h2"]
+                src["down_proj"] = o["up_proj"]
+            e0 = e1 = None
+            if ev is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            q.qerl_nvfp4_lora_linear_fwd(src[name], codes, scales, ts, A, B, self.wl.lora_scale, y=o[name],
+                                         ws=buf["ws"])
+            if ev is not None:
+                e1.record()
+                ev.setdefault(name, []).append((e0, e1))
+        return o["down_proj"]
+
+
+def run_ours(args, rank, world, local_rank):
+    import nvfp4_weight_only_quantize_gb300 as q
+    from nvfp4_weight_only_quantize_gb300 import synth
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = synth.WORKLOADS[1]
+    M = args.M
+    per_copy = sum(N * K * 0.5625 for _, N, K in wl.linears)
+    n_copies = max(2, int(3 * L2_BYTES // per_copy) + 1)
+    layer = DecodeLayer(wl, n_copies, dev)
+    buf = layer.buffers(M, dev)
+    x = synth.activations(M, wl.hidden, synth.seed_of(1, 0, synth.T_X), dev)
+    attn = synth.activations(M, wl.hidden, synth.seed_of(1, 1, synth.T_X), dev)
+    sigma = q.qerl_aqn_sigma(0, 1000, wl.sigma[0], wl.sigma[1], 10)
+
+    for i in range(args.warmup):
+        layer.step(i % n_copies, x, attn, buf, sigma, i)
+    torch.cuda.synchronize()
+    assert q.get_error() == 0
+
+    # --- device-resident timed region
+    ev = {}
+    clocks = ClockSampler(torch.cuda.current_device()).start()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = q.launch_count()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        layer.step(i % n_copies, x, attn, buf, sigma, i, ev=ev)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    launches = q.launch_count() - n0
+    clk = clocks.stop()
+    secs = t0.elapsed_time(t1) / 1e3
+    max_secs, total_units = combine_ranks(secs, layer.bytes_per_step * args.steps)
+    value = total_units / max_secs / 1e9
+
+    per_linear = {}
+    for name, N, K in wl.linears:
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev[name])
+        per_linear[name] = {"us": round(ms * 1e3, 2), "GBps": round(linear_bytes(N, K, wl.r) / (ms / 1e3) / 1e9, 1)}
+
+    # --- end to end through the public API with host buffers
+    xh = x.cpu().pin_memory()
+    ah = attn.cpu().pin_memory()
+    yh = torch.empty(M, wl.hidden, dtype=torch.bfloat16).pin_memory()
+    xd, ad = torch.empty_like(x), torch.empty_like(attn)
+    for i in range(2):
+        xd.copy_(xh, non_blocking=True)
+        ad.copy_(ah, non_blocking=True)
+        yh.copy_(layer.step(i % n_copies, xd, ad, buf, sigma, i), non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        xd.copy_(xh, non_blocking=True)
+        ad.copy_(ah, non_blocking=True)
+        yh.copy_(layer.step(i % n_copies, xd, ad, buf, sigma, i), non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_secs, e2e_units = combine_ranks(e0.elapsed_time(e1) / 1e3, layer.bytes_per_step * args.steps)
+
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    dom = "gate_proj"
+    dN, dK = [(N, K) for n, N, K in wl.linears if n == dom][0]
+    ach = linear_bytes(dN, dK, wl.r) / (per_linear[dom]["us"] / 1e6) / 1e9
+    ms_step = max_secs / args.steps * 1e3
+    line = {
+        "metric": "NVFP4+LoRA linear decode HBM GB/s (Qwen2.5-7B decoder layer)",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 activations, nvfp4 weights, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": wl.name + f"; step at M={M}", "tokens_per_step": M, "lora_rank": wl.r,
+                   "layer_copies_rotated": n_copies,
+                   "l2": f"inputs larger than L2: {n_copies} rotating layer copies, "
+                         f"{n_copies * per_copy / 2**20:.0f} MiB NVFP4 > 129 MiB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(M * args.steps * world / max_secs, 1),
+        "pct_of_hbm_peak": round(100 * value / world / hbm, 2),
+        "per_linear": per_linear,
+        "roofline": {"bound": "hbm", "kernel": f"linear fwd {dom} {dN}x{dK} (M={M}, r={wl.r})",
+                     "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None},
+        "e2e": {"value": round(e2e_units / e2e_secs / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * M * wl.hidden * 2, "d2h_bytes_per_step": M * wl.hidden * 2},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, M, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ oracle arm
+_ORACLE_INPUTS = {}
+
+
+def _oracle_linear_sample(wl, lin_idx, rows=1):
+    """Quantize one linear and run `rows` token rows of the forward with the oracle;
+    returns (seconds, NVFP4+LoRA bytes of that linear)."""
+    import numpy as np
+    import oracle
+    from nvfp4_weight_only_quantize_gb300 import synth
+    name, N, K = wl.linears[lin_idx]
+    key = (lin_idx, rows)
+    if key not in _ORACLE_INPUTS:  # inputs and the quantized weight are prepared once, untimed
+        base = synth.seed_of(1, 0, 16 * lin_idx)
+        rc, codes, scales, st = oracle.nvfp4_quantize(synth.bits(synth.weight(N, K, base + synth.T_W)))
+        _ORACLE_INPUTS[key] = (synth.bits(synth.activations(rows, K, base + synth.T_X)), codes, scales, st,
+                               synth.bits(synth.lora_A(wl.r, K, base + synth.T_A)),
+                               synth.bits(synth.lora_B(N, wl.r, base + synth.T_B)))
+    xb, codes, scales, st, Ab, Bb = _ORACLE_INPUTS[key]
+    t = time.perf_counter()
+    oracle.lora_linear_fwd(xb, codes, scales, st, Ab, Bb, wl.lora_scale, rows=np.arange(rows))
+    return time.perf_counter() - t, linear_bytes(N, K, wl.r)
+
+
+def cpu_baseline(wl, M, budget_s=20.0):
+    """The oracle forward on a bounded sample of the decode layer: one token row
+    through the linears (cycling q..down) until ~budget_s of CPU work; the
+    throughput is scaled to the M-token step (time x M)."""
+    secs = byts = 0.0
+    n = 0
+    while secs < budget_s and n < 7 * 4:
+        s, b = _oracle_linear_sample(wl, n % 7)
+        secs, byts, n = secs + s, byts + b, n + 1
+    return {"value": round(byts / (secs * M) / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} linear forwards of 1 token row (cycling q..down of the 7B layer), "
+                      f"{secs:.1f} s of single-thread fp64 oracle; time scaled x{M} to the M={M} step"}
+
+
+def run_reference(args, rank, world):
+    from nvfp4_weight_only_quantize_gb300 import synth
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[1]
+    M = args.M
+    for i in range(args.warmup):
+        _oracle_linear_sample(wl, i % 7)
+    secs = byts = 0.0
+    for i in range(args.steps):
+        s, b = _oracle_linear_sample(wl, i % 7)
+        secs, byts = secs + s, byts + b
+    value = byts / (secs * M) / 1e9
+    line = {"impl": "reference", "metric": "NVFP4+LoRA linear decode HBM GB/s (Qwen2.5-7B decoder layer)",
+            "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * M * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": wl.name + f"; step at M={M}", "tokens_per_step": M, "lora_rank": wl.r},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "each step: the CPU oracle forward of 1 token row through one linear of "
+                                       f"the 7B layer (cycling q..down), time scaled x{M} to the M={M} step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--M", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local_rank = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        import nvfp4_weight_only_quantize_gb300 as q
+        q.lib()  # the CUDA library must be built; no fallback
+        run_ours(args, rank, world, local_rank)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * qerl.h -- C ABI of the GB300 (sm_103a) NVFP4 weight-only LoRA linear library.
+ *
+ * What it computes (sources are web pages about QeRL, cited by title/section):
+ *  - "QeRL: NVFP4-Quantized Reinforcement Learning -- Redefining Efficiency in AI
+ *    Training and Inference" (bitsofall), section "NVFP4: NVIDIA's FP4 Format":
+ *    16-element blocks along a row, an FP8 E4M3 scale per block plus one FP32
+ *    tensor scale (about 4.5 bits per weight), block scale = round_up(amax/vmax),
+ *    element = round_to_even(value/scale).  Same page, LoRA paragraph and
+ *    "Implementation and Practical Details": a frozen quantized W plus a
+ *    trainable low-rank adapter in higher precision; weight-only quantization,
+ *    activations and gradients stay high precision.
+ *  - "QERL: NVFP4-intensive learning (RL) brings 32B LLM training to H100"
+ *    (dataforcee), sections on the RL loop and on AQN: weight-only FP4 with
+ *    FP4 x BF16 kernels; AQN adds channel-wise Gaussian noise to the norm's scale
+ *    parameters under an exponential schedule.
+ *  - "QeRL: Beyond Efficiency -- Quantization-enhanced Reinforcement Learning for
+ *    LLMs" (1kpapers), summary: channel-wise Gaussian noise via the norm layer,
+ *    exponential decay.  "QeRL" README mirror, "Hints for QeRL training" 2-3:
+ *    prefill still dequantizes; sigma_start, sigma_end, num_stages.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked (device) are CUDA device pointers on the current device;
+ *    (host) pointers are host memory.  The caller owns and allocates every
+ *    buffer, including workspaces; the library allocates nothing per call.
+ *  - All matrices are dense row-major.  bf16 buffers are 16-bit IEEE bfloat16.
+ *  - Work is enqueued asynchronously on `stream` (NULL = legacy default stream).
+ *    Calls never synchronize, except qerl_get_error.
+ *  - Argument errors are returned synchronously and nothing is launched.  Errors
+ *    found by kernels (non-finite weights, a bounded wait that ran out) are
+ *    latched on the device and reported by qerl_get_error.
+ *  - The library runs only on compute capability 10.3 (GB300); elsewhere every
+ *    launching call returns QERL_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef QERL_H
+#define QERL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *qerl_stream_t;
+
+typedef enum {
+    QERL_OK = 0,
+    QERL_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad flag */
+    QERL_ERR_SHAPE = 2,              /* K % 16 != 0, r out of [1, 256], ... */
+    QERL_ERR_ALIGN = 3,              /* a pointer or row stride not 16-byte aligned */
+    QERL_ERR_NONFINITE = 4,          /* the weight held an Inf or NaN (latched) */
+    QERL_ERR_CUDA = 5,               /* a CUDA runtime call failed */
+    QERL_ERR_TIMEOUT = 6,            /* a bounded device-side wait ran out (latched) */
+    QERL_ERR_UNSUPPORTED_DEVICE = 7, /* current device is not compute capability 10.3 */
+    QERL_ERR_WORKSPACE = 8           /* workspace missing or smaller than required */
+} qerl_status;
+
+/* Block-scale rounding of the quantizer. */
+enum { QERL_SCALE_ROUND_UP = 0, QERL_SCALE_ROUND_NEAREST_EVEN = 1 };
+
+typedef struct {
+    int scale_round; /* QERL_SCALE_ROUND_UP (default) or QERL_SCALE_ROUND_NEAREST_EVEN */
+} qerl_quant_opts;
+
+/* Operations for qerl_workspace_bytes. */
+enum {
+    QERL_OP_QUANTIZE = 0,
+    QERL_OP_LINEAR_FWD = 1,
+    QERL_OP_LINEAR_BWD = 2,
+    QERL_OP_AQN_RMSNORM = 3
+};
+
+/* Linear algorithm selection (qerl_set_linear_algo); AUTO is the default. */
+enum { QERL_ALGO_AUTO = 0, QERL_ALGO_SIMT = 1, QERL_ALGO_TCGEN05 = 2 };
+
+/*
+ * NVFP4 quantization of a bf16 weight (bitsofall, "NVFP4: NVIDIA's FP4 Format":
+ * two-level scaling, cuDNN block-scaling recipe).
+ *   W            (device) bf16 [N, K], row stride ldw elements (ldw >= K,
+ *                ldw*2 and W 16-byte aligned).
+ *   codes        (device) out, uint8 [N, K/2]: element 2j of a row in bits 0-3 of
+ *                byte j, element 2j+1 in bits 4-7; E2M1 code = sign bit 3,
+ *                magnitude index 0..7 of {0, .5, 1, 1.5, 2, 3, 4, 6}; zero is 0x0.
+ *   scales       (device) out, uint8 [N, K/16] E4M3 block scales, row-major.
+ *   tensor_scale (device) out, one float: s_t = amax|W| / (6*448), 1.0 if W == 0.
+ *   Block scale = smallest E4M3 >= amax_block / (6*s_t) (or nearest-even with
+ *   opts->scale_round), saturated at 448; code = nearest E2M1 of
+ *   w / (scale*s_t), ties to the even code, saturated at 6.
+ *   Dequantized weight: w_hat = e2m1(code) * e4m3(scale) * s_t.
+ *   opts may be NULL (round up).  ws (device) >= qerl_workspace_bytes(
+ *   QERL_OP_QUANTIZE, 0, N, K, 0) bytes of scratch, contents on entry ignored.
+ *   K % 16 == 0 required (QERL_ERR_SHAPE).  An Inf/NaN in W latches
+ *   QERL_ERR_NONFINITE, sets *tensor_scale to NaN and leaves codes/scales
+ *   undefined.
+ */
+qerl_status qerl_nvfp4_quantize(const void *W, int64_t N, int64_t K, int64_t ldw,
+                                uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                                const qerl_quant_opts *opts, void *ws, size_t ws_bytes,
+                                qerl_stream_t stream);
+
+/*
+ * Dequantization (test aid; bitsofall "NVFP4" section): W_out (device) bf16
+ * [N, K] = e2m1(code) * e4m3(scale), times *tensor_scale when
+ * apply_tensor_scale != 0 (then rounded to nearest-even bf16; without it the
+ * product is exact in bf16).  Inputs as produced by qerl_nvfp4_quantize.
+ */
+qerl_status qerl_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales,
+                                  const float *tensor_scale, int64_t N, int64_t K,
+                                  void *W_out, int apply_tensor_scale, qerl_stream_t stream);
+
+/*
+ * Forward of the frozen NVFP4 linear with its LoRA adapter (bitsofall, LoRA
+ * paragraph and "Implementation and Practical Details"; dataforcee, RL-loop
+ * section: weight-only FP4 x BF16):
+ *     y = x * w_hat^T + lora_scale * (x * A^T) * B^T
+ *   x      (device) bf16 [M, K]        A (device) bf16 [r, K]
+ *   codes/scales/tensor_scale (device) NVFP4 weight of shape [N, K]
+ *   B      (device) bf16 [N, r]        y (device) out bf16 [M, N]
+ *   t_out  (device) optional out float [M, r] = x * A^T (for the backward); NULL ok
+ *   Accumulation is FP32; the result is rounded to bf16 once.  1 <= r <= 256,
+ *   K % 16 == 0, M, N >= 1; x, A, B, y and the codes rows 16-byte aligned
+ *   (K % 32 == 0 for the tensor-core path, else the CUDA-core path runs).
+ *   ws (device) >= qerl_workspace_bytes(QERL_OP_LINEAR_FWD, M, N, K, r).
+ */
+qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
+                                       const uint8_t *codes, const uint8_t *scales,
+                                       const float *tensor_scale, const void *A, const void *B,
+                                       int r, float lora_scale, void *y, float *t_out,
+                                       void *ws, size_t ws_bytes, qerl_stream_t stream);
+
+/*
+ * Backward through the frozen NVFP4 weight into the LoRA adapter (bitsofall,
+ * "Implementation and Practical Details": gradients flow through dequantized
+ * weights; W itself is frozen so there is no dW):
+ *     v  = dy * B                                   (FP32, internal)
+ *     dx = dy * w_hat + lora_scale * v * A          (bf16 out [M, K])
+ *     dA = lora_scale * v^T * x                     (float out [r, K])
+ *     dB = lora_scale * dy^T * (x * A^T)            (float out [N, r])
+ *   dy (device) bf16 [M, N]; x (device) bf16 [M, K]; t_saved (device) optional
+ *   float [M, r] = x * A^T from the forward (recomputed when NULL).
+ *   accumulate_grads != 0 adds into dA/dB instead of overwriting.  dx, dA or dB
+ *   may be NULL to skip that output.  Shapes/alignment as the forward.
+ *   ws (device) >= qerl_workspace_bytes(QERL_OP_LINEAR_BWD, M, N, K, r).
+ */
+qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x, int64_t M, int64_t K,
+                                       int64_t N, const uint8_t *codes, const uint8_t *scales,
+                                       const float *tensor_scale, const void *A, const void *B,
+                                       int r, float lora_scale, const float *t_saved, void *dx,
+                                       float *dA, float *dB, int accumulate_grads, void *ws,
+                                       size_t ws_bytes, qerl_stream_t stream);
+
+/*
+ * AQN-RMSNorm (1kpapers summary; dataforcee AQN paragraph: channel-wise
+ * Gaussian noise in the norm's scale parameters):
+ *     y[m, c] = x[m, c] / sqrt(mean_c x[m, :]^2 + eps) * (gamma[c] + sigma * z[c])
+ *   x (device) bf16 [M, H], gamma (device) bf16 [H], y (device) out bf16 [M, H].
+ *   z[c] ~ N(0, 1) is one vector per (seed, step, layer_id), shared by all M
+ *   tokens: Philox4x64-10 with key (seed, layer_id), counter (c/4, step, 0, 0),
+ *   Box-Muller on word pairs (see qerl_aqn_noise).  sigma == 0 is plain RMSNorm.
+ *   ws (device) >= qerl_workspace_bytes(QERL_OP_AQN_RMSNORM, M, 0, H, 0).
+ */
+qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
+                             float sigma, uint64_t seed, uint64_t step, uint32_t layer_id,
+                             void *y, void *ws, size_t ws_bytes, qerl_stream_t stream);
+
+/*
+ * The AQN noise vector alone (test aid): z_out (device) float [H]; raw_out
+ * (device, optional) uint64 [H], the Philox word each channel used:
+ * block i = c/4 -> words w0..w3 of Philox4x64-10(counter (i, step, 0, 0),
+ * key (seed, layer_id)); z[4i], z[4i+1] from (w0, w1) and z[4i+2], z[4i+3]
+ * from (w2, w3) with u1 = ((wa >> 11) + 1) * 2^-53, u2 = (wb >> 11) * 2^-53,
+ * z = sqrt(-2 ln u1) * (cos 2 pi u2, sin 2 pi u2); raw_out[c] = w_(c mod 4).
+ */
+qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, uint32_t layer_id,
+                           float *z_out, uint64_t *raw_out, qerl_stream_t stream);
+
+/*
+ * Noise schedule (host function; "QeRL" README "Hints" item 3, 1kpapers
+ * summary: exponential decay): num_stages equal stages over total_steps;
+ * stage k = min(floor(step * num_stages / total_steps), num_stages - 1);
+ * sigma = sigma_start * (sigma_end / sigma_start)^(k / (num_stages - 1)).
+ * num_stages <= 1 or total_steps <= 0 returns sigma_start.
+ */
+float qerl_aqn_sigma(int64_t step, int64_t total_steps, float sigma_start, float sigma_end,
+                     int num_stages);
+
+/* Scratch bytes an operation needs (0 if none).  Sizes as in the calls. */
+size_t qerl_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int r);
+
+/* Waits for `stream`, then returns (and clears) the first error latched by a
+ * kernel on the current device, or a CUDA error, or QERL_OK. */
+qerl_status qerl_get_error(qerl_stream_t stream);
+
+/* Static description of a status code. */
+const char *qerl_status_string(qerl_status status);
+
+/* Selects the linear kernels (process-wide): QERL_ALGO_AUTO, _SIMT or _TCGEN05.
+ * TCGEN05 falls back to SIMT for shapes it does not cover. */
+qerl_status qerl_set_linear_algo(int algo);
+
+/* Number of kernels this library launched since load (host-side counter). */
+uint64_t qerl_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QERL_H */

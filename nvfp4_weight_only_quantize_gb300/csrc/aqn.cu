@@ -1,0 +1,182 @@
+// Adaptive Quantization Noise (AQN) RMSNorm.
+//
+// 1kpapers summary of "QeRL: Beyond Efficiency": AQN injects channel-wise
+// Gaussian noise via the normalization layer with an exponential decay
+// schedule; dataforcee "QERL: NVFP4-intensive learning" AQN paragraph: the noise
+// lives in the norm's scale parameters.  So the norm uses gamma + sigma * z with
+// one z[H] ~ N(0, 1) per (seed, step, layer), shared by every token.
+//
+// Two kernels: (1) the noise and the noisy scale vector, H/4 threads, each one
+// Philox4x64-10 block and two Box-Muller pairs in double precision; (2) the
+// bandwidth-bound RMSNorm, one CTA per token row.
+#include "common.cuh"
+
+namespace qerl {
+namespace {
+
+// Philox4x64-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11): ten rounds of two 64x64->128-bit products with the published
+// multipliers; the key is bumped by the Weyl constants after every round.
+__device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1)
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t a0 = 0xD2E7470EE14C6C93ull * c[0], h0 = __umul64hi(0xD2E7470EE14C6C93ull, c[0]);
+        const uint64_t a1 = 0xCA5A826395121157ull * c[2], h1 = __umul64hi(0xCA5A826395121157ull, c[2]);
+        const uint64_t n0 = h1 ^ c[1] ^ k0, n2 = h0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = a1;
+        c[2] = n2;
+        c[3] = a0;
+        k0 += 0x9E3779B97F4A7C15ull;
+        k1 += 0xBB67AE8584CAA73Bull;
+    }
+}
+
+// z for channels 4i..4i+3; writes any of z_out / raw_out / scale_out given.
+__global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32_t layer,
+                                 const __nv_bfloat16 *__restrict__ gamma, float sigma, float *__restrict__ scale_out,
+                                 float *__restrict__ z_out, uint64_t *__restrict__ raw_out)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i * 4 >= H) return;
+    uint64_t w[4] = {(uint64_t)i, step, 0ull, 0ull};
+    philox4x64_10(w, seed, (uint64_t)layer);
+    double z[4];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const double u1 = ((double)(w[2 * p] >> 11) + 1.0) * 0x1p-53;  // (0, 1]
+        const double u2 = (double)(w[2 * p + 1] >> 11) * 0x1p-53;      // [0, 1)
+        const double rad = sqrt(-2.0 * log(u1));
+        double sn, cs;
+        sincospi(2.0 * u2, &sn, &cs);
+        z[2 * p] = rad * cs;
+        z[2 * p + 1] = rad * sn;
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int64_t c = 4 * i + p;
+        if (c >= H) break;
+        if (z_out) z_out[c] = (float)z[p];
+        if (raw_out) raw_out[c] = w[p];
+        if (scale_out) scale_out[c] = (float)((double)bf16f(gamma[c]) + (double)sigma * z[p]);
+    }
+}
+
+constexpr int kNormThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// y = x * rsqrt(mean(x^2) + eps) * g, g = noisy scale (float) or gamma (bf16).
+// Rows are strided over the grid; 16-byte vectors when H % 8 == 0.
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t H, const float *__restrict__ gscale,
+                   const __nv_bfloat16 *__restrict__ gamma, float eps, __nv_bfloat16 *__restrict__ y)
+{
+    __shared__ float red[32];
+    const bool vec = (H % 8) == 0;
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const __nv_bfloat16 *row = x + m * H;
+        __nv_bfloat16 *out = y + m * H;
+        float ss = 0.0f;
+        if (vec) {
+            for (int64_t v = threadIdx.x; v < H / 8; v += blockDim.x) {
+                const uint4 u = reinterpret_cast<const uint4 *>(row)[v];
+                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float a = bf16lo(wd[i]), b = bf16hi(wd[i]);
+                    ss = fmaf(a, a, ss);
+                    ss = fmaf(b, b, ss);
+                }
+            }
+        } else {
+            for (int64_t c = threadIdx.x; c < H; c += blockDim.x) {
+                const float a = bf16f(row[c]);
+                ss = fmaf(a, a, ss);
+            }
+        }
+        ss = block_sum(ss, red);
+        const float inv = rsqrtf(ss / (float)H + eps);
+        if (vec) {
+            for (int64_t v = threadIdx.x; v < H / 8; v += blockDim.x) {
+                const uint4 u = reinterpret_cast<const uint4 *>(row)[v];
+                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t c = v * 8 + 2 * i;
+                    const float g0 = gscale ? gscale[c] : bf16f(gamma[c]);
+                    const float g1 = gscale ? gscale[c + 1] : bf16f(gamma[c + 1]);
+                    const __nv_bfloat162 p = __floats2bfloat162_rn(bf16lo(wd[i]) * inv * g0, bf16hi(wd[i]) * inv * g1);
+                    o[i] = *reinterpret_cast<const uint32_t *>(&p);
+                }
+                reinterpret_cast<uint4 *>(out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            for (int64_t c = threadIdx.x; c < H; c += blockDim.x) {
+                const float g = gscale ? gscale[c] : bf16f(gamma[c]);
+                out[c] = __float2bfloat16_rn(bf16f(row[c]) * inv * g);
+            }
+        }
+        __syncthreads();  // red[] is reused by the next row
+    }
+}
+
+}  // namespace
+}  // namespace qerl
+
+using namespace qerl;
+
+extern "C" qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, uint32_t layer_id, float *z_out,
+                                      uint64_t *raw_out, qerl_stream_t stream)
+{
+    if (H < 1 || !z_out) return QERL_ERR_INVALID_ARG;
+    QERL_TRY(check_device());
+    const int64_t n = (H + 3) / 4;
+    aqn_noise_kernel<<<(unsigned)((n + 127) / 128), 128, 0, as_cuda(stream)>>>(H, seed, step, layer_id, nullptr,
+                                                                             0.0f, nullptr, z_out, raw_out);
+    return launched();
+}
+
+extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
+                                        float sigma, uint64_t seed, uint64_t step, uint32_t layer_id, void *y,
+                                        void *ws, size_t ws_bytes, qerl_stream_t stream)
+{
+    if (!x || !gamma || !y || M < 0 || H < 1 || !(eps >= 0.0f)) return QERL_ERR_INVALID_ARG;
+    if (M == 0) return QERL_OK;
+    if ((H % 8 == 0) && (!aligned16(x) || !aligned16(y))) return QERL_ERR_ALIGN;
+    const bool noisy = sigma != 0.0f;
+    if (noisy && (!ws || ws_bytes < qerl_workspace_bytes(QERL_OP_AQN_RMSNORM, M, 0, H, 0))) return QERL_ERR_WORKSPACE;
+    QERL_TRY(check_device());
+    cudaStream_t s = as_cuda(stream);
+    float *gscale = nullptr;
+    if (noisy) {
+        gscale = static_cast<float *>(ws);
+        const int64_t n = (H + 3) / 4;
+        aqn_noise_kernel<<<(unsigned)((n + 127) / 128), 128, 0, s>>>(
+            H, seed, step, layer_id, static_cast<const __nv_bfloat16 *>(gamma), sigma, gscale, nullptr, nullptr);
+        QERL_TRY(launched());
+    }
+    int64_t g = M;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    rmsnorm_kernel<<<(unsigned)g, kNormThreads, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), M, H, gscale,
+                                                         static_cast<const __nv_bfloat16 *>(gamma), eps,
+                                                         static_cast<__nv_bfloat16 *>(y));
+    return launched();
+}

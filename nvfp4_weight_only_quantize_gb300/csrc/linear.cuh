@@ -1,0 +1,47 @@
+// Internal interface between the linear entry points and their kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace qerl {
+
+// Arguments of one forward call, validated by the entry point.
+struct FwdArgs {
+    const __nv_bfloat16 *x;
+    int64_t M, K, N;
+    const uint8_t *codes, *scales;
+    const float *tensor_scale;
+    const __nv_bfloat16 *A, *B;
+    int r;
+    float lora_scale;
+    __nv_bfloat16 *y;
+    float *t_out;
+};
+
+struct BwdArgs {
+    const __nv_bfloat16 *dy, *x;
+    int64_t M, K, N;
+    const uint8_t *codes, *scales;
+    const float *tensor_scale;
+    const __nv_bfloat16 *A, *B;
+    int r;
+    float lora_scale;
+    const float *t_saved;
+    __nv_bfloat16 *dx;
+    float *dA, *dB;
+    int accumulate;
+};
+
+size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+
+// Tensor-core (tcgen05) path.  Returns QERL_ERR_SHAPE, having launched nothing,
+// when it does not cover the call; the caller then runs the CUDA-core path.
+size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s);
+qerl_status tc_linear_bwd(const BwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s);
+
+inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+}  // namespace qerl

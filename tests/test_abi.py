@@ -1,0 +1,74 @@
+"""The C-ABI library loads, exports every symbol include/qerl.h declares, and
+rejects bad arguments on the host before any CUDA call (CPU only)."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import nvfp4_weight_only_quantize_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    q.build()
+    return q.lib()
+
+
+def test_header_symbols_are_exported(L):
+    src = open(os.path.join(ROOT, "include", "qerl.h")).read()
+    declared = set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(qerl_\w+)\s*\(", src, re.M))
+    assert declared == set(q.EXPORTED), declared ^ set(q.EXPORTED)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_workspace(L):
+    for s in range(9):
+        assert q.status_string(s)
+    assert q.workspace_bytes(q.OP_QUANTIZE, 0, 10, 32, 0) >= 4096
+    assert q.workspace_bytes(q.OP_AQN_RMSNORM, 4, 0, 3584, 0) >= 3584 * 4
+    assert q.workspace_bytes(q.OP_LINEAR_FWD, 64, 3584, 3584, 32) >= 64 * 32 * 4
+    assert q.workspace_bytes(q.OP_LINEAR_BWD, 64, 3584, 3584, 32) >= 2 * 64 * 32 * 4
+
+
+def test_argument_errors_return_before_any_launch(L):
+    fake = C.c_void_p(1 << 20)  # never dereferenced: every case fails its host check first
+    ws = C.c_void_p(1 << 20)
+    # quantize: K % 16, null pointers, misaligned row stride, bad rounding flag
+    assert L.qerl_nvfp4_quantize(fake, 4, 24, 24, fake, fake, fake, None, ws, 4096, None) == 2
+    assert L.qerl_nvfp4_quantize(None, 4, 32, 32, fake, fake, fake, None, ws, 4096, None) == 1
+    assert L.qerl_nvfp4_quantize(fake, 4, 32, 36, fake, fake, fake, None, ws, 4096, None) == 3
+    assert L.qerl_nvfp4_quantize(C.c_void_p((1 << 20) + 2), 4, 32, 32, fake, fake, fake, None, ws, 4096,
+                                 None) == 3
+    bad_opts = q._QuantOpts(7)
+    assert L.qerl_nvfp4_quantize(fake, 4, 32, 32, fake, fake, fake, C.byref(bad_opts), ws, 4096, None) == 1
+    assert L.qerl_nvfp4_quantize(fake, 4, 32, 32, fake, fake, fake, None, None, 0, None) == 8
+    # linear: r out of range, K % 16, misaligned x, missing workspace
+    args = lambda x, K, r, wsb: (x, 8, K, 16, fake, fake, fake, fake, fake, r, 2.0, fake, None, ws, wsb, None)
+    assert L.qerl_nvfp4_lora_linear_fwd(*args(fake, 32, 0, 1 << 20)) == 2
+    assert L.qerl_nvfp4_lora_linear_fwd(*args(fake, 32, 257, 1 << 20)) == 2
+    assert L.qerl_nvfp4_lora_linear_fwd(*args(fake, 40, 4, 1 << 20)) == 2
+    assert L.qerl_nvfp4_lora_linear_fwd(*args(C.c_void_p((1 << 20) + 8), 32, 4, 1 << 20)) == 3
+    assert L.qerl_nvfp4_lora_linear_fwd(*args(fake, 32, 4, 0)) == 8
+    bargs = (fake, fake, 8, 32, 16, fake, fake, fake, fake, fake, 4, 2.0, None, fake, fake, fake, 0, ws)
+    assert L.qerl_nvfp4_lora_linear_bwd(*bargs, 0, None) == 8
+    assert L.qerl_nvfp4_lora_linear_bwd(None, *bargs[1:], 1 << 20, None) == 1
+    # AQN
+    assert L.qerl_aqn_rmsnorm(fake, 4, 0, fake, 1e-6, 0.0, 0, 0, 0, fake, ws, 1 << 20, None) == 1
+    assert L.qerl_aqn_rmsnorm(fake, 4, 64, fake, 1e-6, 0.1, 0, 0, 0, fake, None, 0, None) == 8
+    assert L.qerl_aqn_noise(0, 0, 0, 0, fake, None, None) == 1
+    assert L.qerl_set_linear_algo(9) == 1
+
+
+def test_sigma_schedule_matches_oracle(L):
+    for S in (1, 2, 5, 10):
+        for T in (1, 7, 1000):
+            for t in (0, 1, T // 3, T - 1, T, 5 * T):
+                got = q.qerl_aqn_sigma(t, T, 1e-2, 5e-4, S)
+                assert got == pytest.approx(oracle.aqn_sigma(t, T, 1e-2, 5e-4, S), rel=1e-6)
+    assert q.qerl_aqn_sigma(3, 10, 0.0, 1e-3, 4) == 0.0
