@@ -158,8 +158,9 @@ extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, con
                                         float sigma, uint64_t seed, uint64_t step, uint32_t layer_id, void *y,
                                         void *ws, size_t ws_bytes, qerl_stream_t stream)
 {
-    if (!x || !gamma || !y || M < 0 || H < 1 || !(eps >= 0.0f)) return QERL_ERR_INVALID_ARG;
-    if (M == 0) return QERL_OK;
+    if (!gamma || M < 0 || H < 1 || !(eps >= 0.0f)) return QERL_ERR_INVALID_ARG;
+    if (M == 0) return QERL_OK;  // x and y may be NULL for an empty batch
+    if (!x || !y) return QERL_ERR_INVALID_ARG;
     if ((H % 8 == 0) && (!aligned16(x) || !aligned16(y))) return QERL_ERR_ALIGN;
     const bool noisy = sigma != 0.0f;
     if (noisy && (!ws || ws_bytes < qerl_workspace_bytes(QERL_OP_AQN_RMSNORM, M, 0, H, 0))) return QERL_ERR_WORKSPACE;

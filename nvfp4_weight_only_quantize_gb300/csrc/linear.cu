@@ -225,10 +225,10 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int6
                                                   float lora_scale, void *y, float *t_out, void *ws, size_t ws_bytes,
                                                   qerl_stream_t stream)
 {
-    if (!x || !y) return QERL_ERR_INVALID_ARG;
     QERL_TRY(check_common(M, K, N, codes, scales, tensor_scale, A, B, r));
+    if (M == 0) return QERL_OK;  // x, y may be NULL for an empty batch
+    if (!x || !y) return QERL_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y) || (t_out && !aligned16(t_out))) return QERL_ERR_ALIGN;
-    if (M == 0) return QERL_OK;
     if (!ws || ws_bytes < linear_fwd_ws_bytes(M, N, K, r)) return QERL_ERR_WORKSPACE;
     QERL_TRY(check_device());
     const FwdArgs a{static_cast<const __nv_bfloat16 *>(x), M, K, N, codes, scales, tensor_scale,
@@ -249,9 +249,9 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x,
                                                   float *dB, int accumulate_grads, void *ws, size_t ws_bytes,
                                                   qerl_stream_t stream)
 {
-    if (!dy || !x) return QERL_ERR_INVALID_ARG;
     QERL_TRY(check_common(M, K, N, codes, scales, tensor_scale, A, B, r));
-    if (!aligned16(dy) || !aligned16(x) || (dx && !aligned16(dx)) || (dA && !aligned16(dA)) ||
+    if (M > 0 && (!dy || !x)) return QERL_ERR_INVALID_ARG;
+    if ((M > 0 && (!aligned16(dy) || !aligned16(x))) || (dx && !aligned16(dx)) || (dA && !aligned16(dA)) ||
         (dB && !aligned16(dB)) || (t_saved && !aligned16(t_saved)))
         return QERL_ERR_ALIGN;
     if (M == 0) {  // empty sums: dA = 0, dB = 0 unless accumulating

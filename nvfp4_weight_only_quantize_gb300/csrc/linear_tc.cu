@@ -1,11 +1,689 @@
-// Tensor-core (tcgen05) path of the NVFP4 LoRA linear.
+// Tensor-core (tcgen05) path of the NVFP4 LoRA linear, sm_103a.
+//
+// Swap-AB formulation: the weight is the MMA's 128-row A operand and the
+// tokens are its N side, so one kernel serves decode (M = 1..64 tokens, N
+// padded to 16) and prefill (M in the thousands, 256-token tiles):
+//     D[n, m] = sum_k w''[n, k] * x[m, k] + sum_j B[n, j] * u[m, j]
+//     y[m, n] = bf16(ysc * D[n, m]),   ysc = s_t * 2^c
+// with w'' = e2m1(code) * e4m3(scale) * 2^-c, exact in bf16, and the LoRA
+// down-projection folded in as extra K steps: u = bf16(s * (x A^T) / ysc).
+// The exponent offset c is derived from s_t so that w'' and u are normal bf16
+// numbers and ysc is finite (see tc_exponent_offset).
+//
+// Warp roles (352 threads, one CTA per SM):
+//   warps 0-7  dequantize: packed codes (smem) + scales (global) -> bf16 A tile
+//              in the 128-byte-swizzled K-major layout; warps 0-3 also run the
+//              epilogue (TMEM -> registers -> y, or split-K partials).
+//   warp 8     TMA producer of the packed codes (deep ring, streamed once).
+//   warp 9     TMA producer of the token tile (x, then u for the LoRA steps).
+//   warp 10    allocates TMEM; lane 0 issues tcgen05.mma and the commits.
+// Every mbarrier wait is bounded by a deadline; on expiry the CTA latches
+// QERL_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
+// drained (bounded), TMEM is freed and the CTA exits.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
 #include "linear.cuh"
+#include "sm100_ptx.cuh"
 
 namespace qerl {
+namespace {
 
-size_t tc_fwd_ws_bytes(int64_t, int64_t, int64_t, int) { return 0; }
+using namespace ptx;
+
+constexpr int BK = 64;          // k per stage: one 128-byte swizzle row of bf16
+constexpr int TILE_N = 128;     // weight rows per CTA (MMA M)
+constexpr int NUM_DQ_WARPS = 8;
+constexpr int WARP_RAW = 8, WARP_X = 9, WARP_MMA = 10;
+constexpr int NUM_THREADS = 11 * 32;
+constexpr int RAW_STAGE = 4096;  // 128 rows x 32 code bytes, stored as [2][128][16]
+constexpr int A_BYTES = TILE_N * BK * 2;
+
+template <int BN>
+struct Cfg {
+    static constexpr int S = BN >= 256 ? 3 : 4;                         // dequantized A-tile stages
+    static constexpr int XS = BN >= 256 ? 3 : (BN >= 128 ? 4 : 8);      // token-tile stages
+    static constexpr int R = BN >= 128 ? 8 : (BN >= 64 ? 12 : 16);      // packed-code stages
+    static constexpr int X_BYTES = BN * BK * 2;
+    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+    static constexpr int BAR_BYTES = 1024;
+    static constexpr int SMEM = S * A_BYTES + XS * X_BYTES + R * RAW_STAGE + BAR_BYTES + 1024;
+};
+
+struct TcFwdParams {
+    int M, N, K;
+    int nk;              // K / BK main steps
+    int lora_steps;      // ceil(r / BK)
+    int r, r_pad;        // rank, u row length (lora_steps * BK)
+    int splits, steps_per_split;
+    int n_tiles, m_tiles;
+    const uint8_t *scales;
+    const __nv_bfloat16 *Bl;
+    const float *tensor_scale;
+    __nv_bfloat16 *y;
+    float *partial;
+    uint32_t *counters;
+    unsigned int *err;
+    unsigned long long timeout_ns;
+    int fault;           // test hook: CTA 0 withholds one arrival so its waits time out
+};
+
+// Exponent offset c in [7, 116] with s_t * 2^c in [1, 2) when possible: the
+// dequantized e2m1*e4m3*2^-c then lies in [2^-10-c, 2688*2^-c], a normal bf16
+// range, and the scale factor e4m3 * 2^(126-c) stays finite.
+__device__ __forceinline__ int tc_exponent_offset(float s_t)
+{
+    int e = 0;
+    frexpf(s_t, &e);
+    int c = 1 - e;
+    return c < 7 ? 7 : (c > 116 ? 116 : c);
+}
+
+// 2^e as a float for e in the normal range (exact, unlike exp2f).
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// bf16x2 {f, f} with f = e4m3(b) * 2^(126 - c): exact (<= 4 significant bits).
+__device__ __forceinline__ uint32_t scale_factor_bf16x2(uint32_t b, float pow2)
+{
+    const uint32_t h = __float_as_uint(e4m3_to_float(b) * pow2) >> 16;
+    return h | (h << 16);
+}
+
+// Eight E2M1 codes (one word, element 2j in the low nibble of byte j) -> four
+// bf16x2 words {elem 2j, elem 2j+1}.  The sign goes to bit 15 and the three
+// exponent/mantissa bits to bits 8..6, which as a bf16 is e2m1 * 2^-126 (the
+// code 0.5 becomes the subnormal 2^-127); one bf16x2 multiply by the block's
+// scale factor then gives e2m1 * e4m3 * 2^-c exactly.
+__device__ __forceinline__ void dequant_word(uint32_t q, uint32_t f2, uint32_t *out)
+{
+    const uint32_t q4 = q << 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // byte 1 <- byte j of q4 (its high nibble is element 2j), byte 3 <- byte j of q
+        const uint32_t u = prmt(q4, q, 0x4400u + 0x1111u * (uint32_t)j);
+        const uint32_t raw = (u & 0x80008000u) | ((u >> 6) & 0x01C001C0u);
+        out[j] = bf16x2_mul(raw, f2);
+    }
+}
+
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p)
+{
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap x_map,
+                  const __grid_constant__ CUtensorMap u_map, const TcFwdParams p)
+{
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *A_ring = smem;
+    uint8_t *X_ring = A_ring + C::S * A_BYTES;
+    uint8_t *R_ring = X_ring + C::XS * C::X_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(R_ring + C::R * RAW_STAGE);
+    uint64_t *raw_full = bars;
+    uint64_t *raw_empty = raw_full + C::R;
+    uint64_t *x_full = raw_empty + C::R;
+    uint64_t *x_empty = x_full + C::XS;
+    uint64_t *a_full = x_empty + C::XS;
+    uint64_t *a_empty = a_full + C::S;
+    uint64_t *acc_full = a_empty + C::S;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x % p.splits;
+    const int tile = blockIdx.x / p.splits;
+    const int n_tile = tile % p.n_tiles, m_tile = tile / p.n_tiles;
+    const int n0 = n_tile * TILE_N, m0 = m_tile * BN;
+    const int k_begin = split * p.steps_per_split;
+    const int k_end = min(p.nk, k_begin + p.steps_per_split);
+    const int n_main = k_end > k_begin ? k_end - k_begin : 0;
+    const int n_steps = n_main + (split == p.splits - 1 ? p.lora_steps : 0);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::R; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], NUM_DQ_WARPS);
+        }
+        for (int i = 0; i < C::XS; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
+        }
+        for (int i = 0; i < C::S; ++i) {
+            mbar_init(&a_full[i], NUM_DQ_WARPS);
+            mbar_init(&a_empty[i], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_RAW && lane == 0) prefetch_tensormap(&codes_map);
+    if (warp == WARP_X && lane == 0) {
+        prefetch_tensormap(&x_map);
+        prefetch_tensormap(&u_map);
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const unsigned long long deadline = globaltimer_ns() + p.timeout_ns;
+
+    // Bounded wait for the phase with this parity; false once the CTA aborts.
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        for (;;) {
+            if (*abort_flag) return false;
+            if (mbar_try_wait(bar, parity)) return true;
+            if (globaltimer_ns() > deadline) {
+                *abort_flag = 1;
+                latch_error(p.err, QERL_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    };
+    // Wait used while draining after an abort: ignores the flag, short bound.
+    auto drain_wait = [&](uint64_t *bar, uint32_t parity) {
+        const unsigned long long until = globaltimer_ns() + 100000000ull;  // 100 ms
+        while (!mbar_try_wait(bar, parity) && globaltimer_ns() < until) {
+        }
+    };
+
+    if (warp == WARP_RAW) {
+        // ---------------------------------------------------------- packed codes
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < n_main; ++i) {
+                const int slot = i % C::R;
+                const uint32_t round = (uint32_t)(i / C::R);
+                if (round > 0 && !wait(&raw_empty[slot], (round - 1) & 1u)) break;
+                mbar_arrive_expect_tx(&raw_full[slot], RAW_STAGE);
+                const int kb = (k_begin + i) * (BK / 2);
+                uint8_t *dst = R_ring + slot * RAW_STAGE;
+                tma_load_2d_hint(dst, &codes_map, &raw_full[slot], kb, n0, pol);
+                tma_load_2d_hint(dst + 2048, &codes_map, &raw_full[slot], kb + 16, n0, pol);
+                issued = i + 1;
+            }
+            if (*abort_flag)  // let the copies already issued land before the CTA exits
+                for (int i = issued > C::R ? issued - C::R : 0; i < issued; ++i)
+                    drain_wait(&raw_full[i % C::R], (uint32_t)(i / C::R) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == WARP_X) {
+        // ---------------------------------------------------------- token tiles
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            // The token tiles (and u) may be written by the kernel launched just
+            // before this one: wait for it here (no-op without a programmatic
+            // launch dependency).  Weights are static and are streamed before it.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            int issued = 0;
+            for (int i = 0; i < n_steps; ++i) {
+                const int slot = i % C::XS;
+                const uint32_t round = (uint32_t)(i / C::XS);
+                if (round > 0 && !wait(&x_empty[slot], (round - 1) & 1u)) break;
+                mbar_arrive_expect_tx(&x_full[slot], C::X_BYTES);
+                uint8_t *dst = X_ring + slot * C::X_BYTES;
+                if (i < n_main)
+                    tma_load_2d_hint(dst, &x_map, &x_full[slot], (k_begin + i) * BK, m0, pol);
+                else
+                    tma_load_2d_hint(dst, &u_map, &x_full[slot], (i - n_main) * BK, m0, pol);
+                issued = i + 1;
+            }
+            if (*abort_flag)
+                for (int i = issued > C::XS ? issued - C::XS : 0; i < issued; ++i)
+                    drain_wait(&x_full[i % C::XS], (uint32_t)(i / C::XS) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(TILE_N, BN);
+            for (int i = 0; i < n_steps; ++i) {
+                const int s = i % C::S, xs = i % C::XS;
+                if (!wait(&a_full[s], (uint32_t)(i / C::S) & 1u) || !wait(&x_full[xs], (uint32_t)(i / C::XS) & 1u))
+                    break;
+                tc_fence_after();
+                const uint64_t ad = desc_kmajor_sw128(smem_u32(A_ring + s * A_BYTES));
+                const uint64_t bd = desc_kmajor_sw128(smem_u32(X_ring + xs * C::X_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_bf16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&a_empty[s]);
+                umma_commit(&x_empty[xs]);
+            }
+            // Arrives once every MMA issued above has completed (also after an abort).
+            umma_commit(acc_full);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- dequantize
+        const int row = (warp & 3) * 32 + lane;
+        const int khalf = warp >> 2;
+        const int n = n0 + row;
+        const bool row_ok = n < p.N;
+        const uint8_t *srow = p.scales + (size_t)(row_ok ? n : 0) * (size_t)(p.K / 16) + 2 * khalf;
+        const float pow2 = pow2f(126 - tc_exponent_offset(*p.tensor_scale));
+        const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+        uint32_t sc_next = (row_ok && n_main > 0) ? ldg_u16(srow + (size_t)k_begin * 4) : 0u;
+        for (int i = 0; i < n_steps; ++i) {
+            uint32_t out[16];
+            if (i < n_main) {
+                const int rs = i % C::R;
+                if (!__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(i / C::R) & 1u))) break;
+                const uint4 c = ld_shared_v4(smem_u32(R_ring + rs * RAW_STAGE + khalf * 2048 + row * 16));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);
+                const uint32_t sc = sc_next;
+                if (row_ok && i + 1 < n_main) sc_next = ldg_u16(srow + (size_t)(k_begin + i + 1) * 4);
+                const uint32_t f0 = scale_factor_bf16x2(sc & 0xFFu, pow2);
+                const uint32_t f1 = scale_factor_bf16x2(sc >> 8, pow2);
+                dequant_word(c.x, f0, out + 0);
+                dequant_word(c.y, f0, out + 4);
+                dequant_word(c.z, f1, out + 8);
+                dequant_word(c.w, f1, out + 12);
+            } else {
+                // LoRA up-projection rows: B[n, l*64 + khalf*32 .. +31], zero past r.
+                const int j0 = (i - n_main) * BK + khalf * 32;
+                const __nv_bfloat16 *b = p.Bl + (size_t)(row_ok ? n : 0) * p.r + j0;
+                if (row_ok && (p.r & 7) == 0 && j0 + 32 <= p.r) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(b) + q);
+                        out[4 * q] = v.x;
+                        out[4 * q + 1] = v.y;
+                        out[4 * q + 2] = v.z;
+                        out[4 * q + 3] = v.w;
+                    }
+                } else {
+                    const uint16_t *bh = reinterpret_cast<const uint16_t *>(b);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const uint32_t lo = (row_ok && j0 + 2 * q < p.r) ? bh[2 * q] : 0u;
+                        const uint32_t hi = (row_ok && j0 + 2 * q + 1 < p.r) ? bh[2 * q + 1] : 0u;
+                        out[q] = lo | (hi << 16);
+                    }
+                }
+            }
+            const int s = i % C::S;
+            const uint32_t sround = (uint32_t)(i / C::S);
+            if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&a_empty[s], (sround - 1) & 1u))) break;
+            const uint32_t abase = smem_u32(A_ring + s * A_BYTES) + a_row;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t phys = (uint32_t)((khalf * 4 + q) ^ (row & 7));
+                st_shared_v4(abase + phys * 16, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const bool withhold = p.fault && blockIdx.x == 0 && warp == 0 && i == 0;
+            if (lane == 0 && !withhold) mbar_arrive(&a_full[s]);
+        }
+
+        // ---------------------------------------------------------- epilogue
+        if (warp < 4) {
+            const bool ok = __all_sync(0xFFFFFFFFu, wait(acc_full, 0));
+            tc_fence_after();
+            if (ok) {
+                const float st = *p.tensor_scale;
+                const float ysc = st * pow2f(tc_exponent_offset(st));
+                const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+                if (p.splits == 1) {
+                    for (int c0 = 0; c0 < BN; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + (uint32_t)c0, v);
+                        tmem_wait_ld();
+                        if (row_ok) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int m = m0 + c0 + j;
+                                if (m < p.M) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(__uint_as_float(v[j]) * ysc);
+                            }
+                        }
+                    }
+                } else {
+                    float *part = p.partial + ((size_t)tile * p.splits + split) * (size_t)(TILE_N * BN);
+                    for (int c0 = 0; c0 < BN; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + (uint32_t)c0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * TILE_N + row, __uint_as_float(v[j]));
+                    }
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (threadIdx.x == 0) {
+                        const unsigned int old = atomicAdd(&p.counters[tile], 1u);
+                        *last_flag = (old == (unsigned int)(p.splits - 1)) ? 1 : 0;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (p.splits > 1 && *last_flag) {
+        // Last split of this tile: the whole CTA sums the partials in split
+        // order (deterministic), four rows per item with 16-byte loads.
+        __threadfence();
+        const float st = *p.tensor_scale;
+        const float ysc = st * pow2f(tc_exponent_offset(st));
+        const float *base = p.partial + (size_t)tile * p.splits * (size_t)(TILE_N * BN);
+        for (int it = threadIdx.x; it < BN * (TILE_N / 4); it += NUM_THREADS) {
+            const int col = it / (TILE_N / 4), rq = (it % (TILE_N / 4)) * 4;
+            const int m = m0 + col;
+            if (m >= p.M) continue;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int s2 = 0; s2 < p.splits; ++s2) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN) +
+                                                                         (size_t)col * TILE_N + rq));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int n = n0 + rq + e;
+                if (n < p.N) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(a4[e] * ysc);
+            }
+        }
+        if (threadIdx.x == 0) p.counters[tile] = 0u;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        if (lane == 0) drain_wait(acc_full, 0);  // every issued MMA has finished (no-op unless aborted)
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// LoRA down-projection for the tensor-core path: t = x A^T (FP32), written as
+// u = bf16(t * s / ysc) into a [M, r_pad] buffer (zeros past r) that the main
+// kernel reads as extra K steps, plus t_out when requested.  One CTA computes
+// MB token rows x JB adapter rows; its 256 threads stride over K in 8-element
+// vectors and the partial sums are reduced in shared memory in a fixed order.
+// CTA 0 also clears the split-K tile counters of the main kernel, which is
+// allowed to start (programmatic launch) while this kernel runs.
+constexpr int LD_THREADS = 256;
+
+template <int MB, int JB>
+__global__ void __launch_bounds__(LD_THREADS)
+    lora_down_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ A, int M, int K, int r,
+                     int r_pad, float s, const float *__restrict__ tensor_scale, float *__restrict__ t_out,
+                     __nv_bfloat16 *__restrict__ u, uint32_t *__restrict__ counters, int n_counters)
+{
+    __shared__ float red[LD_THREADS / 32][MB * JB];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
+    const int jgroups = r_pad / JB;
+    const int m0 = (blockIdx.x / jgroups) * MB, j0 = (blockIdx.x % jgroups) * JB;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float acc[MB][JB];
+#pragma unroll
+    for (int a = 0; a < MB; ++a)
+#pragma unroll
+        for (int b = 0; b < JB; ++b) acc[a][b] = 0.0f;
+    if (j0 < r) {
+#pragma unroll 2
+        for (int k = threadIdx.x * 8; k < K; k += LD_THREADS * 8) {
+            uint4 av[JB], xv[MB];
+#pragma unroll
+            for (int b = 0; b < JB; ++b)
+                av[b] = (j0 + b < r) ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)(j0 + b) * K + k))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int a = 0; a < MB; ++a)
+                xv[a] = (m0 + a < M) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + a) * K + k))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int a = 0; a < MB; ++a) {
+                const uint32_t xw[4] = {xv[a].x, xv[a].y, xv[a].z, xv[a].w};
+#pragma unroll
+                for (int b = 0; b < JB; ++b) {
+                    const uint32_t aw[4] = {av[b].x, av[b].y, av[b].z, av[b].w};
+                    float t = acc[a][b];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        t = fmaf(bf16lo(xw[q]), bf16lo(aw[q]), t);
+                        t = fmaf(bf16hi(xw[q]), bf16hi(aw[q]), t);
+                    }
+                    acc[a][b] = t;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < MB; ++a)
+#pragma unroll
+        for (int b = 0; b < JB; ++b) {
+            float v = acc[a][b];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            if (lane == 0) red[warp][a * JB + b] = v;
+        }
+    __syncthreads();
+    if (threadIdx.x < MB * JB) {
+        const int a = threadIdx.x / JB, b = threadIdx.x % JB;
+        const int m = m0 + a, j = j0 + b;
+        if (m < M) {
+            float t = 0.0f;
+#pragma unroll
+            for (int w = 0; w < LD_THREADS / 32; ++w) t += red[w][threadIdx.x];
+            if (j < r) {
+                const float st = *tensor_scale;
+                const float fac = s / (st * pow2f(tc_exponent_offset(st)));
+                if (t_out) t_out[(size_t)m * r + j] = t;
+                u[(size_t)m * r_pad + j] = __float2bfloat16_rn(t * fac);
+            } else {
+                u[(size_t)m * r_pad + j] = __float2bfloat16_rn(0.0f);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor map: `inner` elements per row (contiguous), `outer` rows.
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct FwdPlan {
+    int BN = 0, n_tiles = 0, m_tiles = 0, splits = 1, sps = 0, nk = 0, lora_steps = 0, r_pad = 0;
+    size_t off_u = 0, off_cnt = 0, off_part = 0, total = 0;
+};
+
+FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
+{
+    FwdPlan pl;
+    pl.BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    pl.n_tiles = (int)((N + TILE_N - 1) / TILE_N);
+    pl.m_tiles = (int)((M + pl.BN - 1) / pl.BN);
+    pl.nk = (int)(K / BK);
+    pl.lora_steps = (r + BK - 1) / BK;
+    pl.r_pad = pl.lora_steps * BK;
+    const int64_t tiles = (int64_t)pl.n_tiles * pl.m_tiles;
+    const int sms = num_sms();
+    int splits = 1;
+    if (tiles < sms) {
+        splits = (int)(sms / tiles);
+        int max_splits = pl.nk / 2 > 0 ? pl.nk / 2 : 1;  // at least two k-steps per split
+        if (max_splits > 16) max_splits = 16;          // bounds the fixup's partial traffic
+        if (splits > max_splits) splits = max_splits;
+        if (splits < 1) splits = 1;
+    }
+    pl.sps = (pl.nk + splits - 1) / splits;
+    pl.splits = (pl.nk + pl.sps - 1) / pl.sps;  // no empty split
+    pl.off_u = 0;
+    pl.off_cnt = round256(size_t(M) * pl.r_pad * 2);
+    pl.off_part = pl.off_cnt + round256(size_t(tiles) * 4);
+    pl.total = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
+    return pl;
+}
+
+bool tc_fwd_applies(int64_t M, int64_t N, int64_t K, int r)
+{
+    return M >= 1 && N >= 1 && K >= BK && K % BK == 0 && r >= 1 && r <= 256 && M <= (1 << 30) &&
+           N <= (1 << 30) && K <= (1 << 30);
+}
+
+struct Env {
+    unsigned long long timeout_ns = 2000000000ull;  // 2 s
+    int fault = 0;
+    Env()
+    {
+        const char *f = std::getenv("QERL_TEST_WITHHOLD_ARRIVAL");
+        if (f && f[0] == '1') {
+            fault = 1;
+            timeout_ns = 50000000ull;  // 50 ms
+        }
+    }
+};
+const Env &env()
+{
+    static Env e;
+    return e;
+}
+
+template <int BN>
+qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const TcFwdParams &p,
+                       unsigned grid, cudaStream_t s)
+{
+    if (cudaFuncSetAttribute(tc_fwd_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) !=
+        cudaSuccess)
+        return QERL_ERR_CUDA;
+    // Programmatic dependent launch: the CTAs may start while the LoRA
+    // down-projection still runs and stream their (static) weights; the token
+    // producer waits for it with griddepcontrol.wait.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tc_fwd_kernel<BN>, cm, xm, um, p) != cudaSuccess) return QERL_ERR_CUDA;
+    return launched();
+}
+
+}  // namespace
+
+size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
+{
+    return tc_fwd_applies(M, N, K, r) ? plan_fwd(M, N, K, r).total : 0;
+}
+
 size_t tc_bwd_ws_bytes(int64_t, int64_t, int64_t, int) { return 0; }
-qerl_status tc_linear_fwd(const FwdArgs &, char *, size_t, cudaStream_t) { return QERL_ERR_SHAPE; }
+
+qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s)
+{
+    if (!tc_fwd_applies(a.M, a.N, a.K, a.r)) return QERL_ERR_SHAPE;
+    const FwdPlan pl = plan_fwd(a.M, a.N, a.K, a.r);
+    if (ws_bytes < pl.total) return QERL_ERR_WORKSPACE;
+    __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u);
+    uint32_t *counters = reinterpret_cast<uint32_t *>(ws + pl.off_cnt);
+    float *partial = reinterpret_cast<float *>(ws + pl.off_part);
+    const int tiles = pl.n_tiles * pl.m_tiles;
+
+    CUtensorMap cm, xm, um;
+    if (!make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, a.K / 2, a.N, a.K / 2, 16, TILE_N,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, a.K * 2, BK, pl.BN,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&um, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, pl.r_pad, a.M, pl.r_pad * 2, BK, pl.BN,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return QERL_ERR_CUDA;
+
+    // 1) LoRA down-projection (+ counter reset)
+    {
+        constexpr int MB = 8, JB = 4;
+        const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
+        lora_down_kernel<MB, JB><<<blocks, LD_THREADS, 0, s>>>(a.x, a.A, (int)a.M, (int)a.K, a.r, pl.r_pad,
+                                                               a.lora_scale, a.tensor_scale, a.t_out, u, counters,
+                                                               tiles);
+        QERL_TRY(launched());
+    }
+
+    // 2) main tensor-core kernel
+    TcFwdParams p;
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.nk = pl.nk;
+    p.lora_steps = pl.lora_steps;
+    p.r = a.r;
+    p.r_pad = pl.r_pad;
+    p.splits = pl.splits;
+    p.steps_per_split = pl.sps;
+    p.n_tiles = pl.n_tiles;
+    p.m_tiles = pl.m_tiles;
+    p.scales = a.scales;
+    p.Bl = a.B;
+    p.tensor_scale = a.tensor_scale;
+    p.y = a.y;
+    p.partial = partial;
+    p.counters = counters;
+    p.err = error_word();
+    p.timeout_ns = env().timeout_ns;
+    p.fault = env().fault;
+    const unsigned grid = (unsigned)(tiles * pl.splits);
+    switch (pl.BN) {
+    case 16: return launch_fwd<16>(cm, xm, um, p, grid, s);
+    case 32: return launch_fwd<32>(cm, xm, um, p, grid, s);
+    case 64: return launch_fwd<64>(cm, xm, um, p, grid, s);
+    case 128: return launch_fwd<128>(cm, xm, um, p, grid, s);
+    default: return launch_fwd<256>(cm, xm, um, p, grid, s);
+    }
+}
+
 qerl_status tc_linear_bwd(const BwdArgs &, char *, size_t, cudaStream_t) { return QERL_ERR_SHAPE; }
 
 }  // namespace qerl

@@ -3,7 +3,10 @@ tolerance checks.  Tolerances:
   - quantized codes, scale bytes, tensor scale, Philox words: bit-exact;
   - linear outputs (y, dx, dA, dB): |got - ref| <= 1e-2 * (|ref| + rms(ref))
     elementwise, rms over the checked outputs;
-  - AQN-RMSNorm: |got - ref| <= 2e-3 * (|ref| + rms(ref)); noise z: 1e-6 absolute.
+  - AQN-RMSNorm: |got - ref| <= 2e-3 * (|ref| + rms(ref)) + ulp_bf16(ref) / 2; the
+    half ulp is the rounding of the bf16 result itself (up to 2^-8 relative), which
+    no bf16 output can avoid and which is larger than 2e-3 in the low part of a
+    binade; noise z: 1e-6 absolute.
 """
 import numpy as np
 import torch
@@ -16,7 +19,13 @@ _QUANT_CACHE = {}  # the oracle's quantization of the 8 most recent weights
 NORM_TOL = 2e-3
 
 
-def assert_rel_rms(got, ref, tol, what=""):
+def half_ulp_bf16(ref):
+    """Half the spacing of bf16 numbers at |ref| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(ref, np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+
+
+def assert_rel_rms(got, ref, tol, what="", bf16_out=False):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
@@ -24,6 +33,8 @@ def assert_rel_rms(got, ref, tol, what=""):
     rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
     err = np.abs(got - ref)
     bound = tol * (np.abs(ref) + rms)
+    if bf16_out:
+        bound = bound + half_ulp_bf16(ref)
     bad = err > bound
     if bad.any():
         i = np.unravel_index(np.argmax(err - bound), err.shape)

@@ -26,7 +26,7 @@ def test_rmsnorm_parity(M, H, sigma):
     g = synth.norm_gamma(H, H + 1).cuda()
     y = q.qerl_aqn_rmsnorm(x, g, 1e-6, sigma, seed=7, step=3, layer_id=2)
     ref = oracle.aqn_rmsnorm(synth.bits(x), synth.bits(g), 1e-6, sigma, 7, 3, 2)
-    assert_rel_rms(f64(y), ref, NORM_TOL, "aqn_rmsnorm")
+    assert_rel_rms(f64(y), ref, NORM_TOL, "aqn_rmsnorm", bf16_out=True)
 
 
 def test_rmsnorm_prefill_size_sampled_rows():
@@ -37,7 +37,7 @@ def test_rmsnorm_prefill_size_sampled_rows():
     y = q.qerl_aqn_rmsnorm(x, g, 1e-6, 1e-2, seed=2, step=5, layer_id=0)
     rows = np.sort(np.random.default_rng(0).choice(M, 64, replace=False))
     ref = oracle.aqn_rmsnorm(synth.bits(x), synth.bits(g), 1e-6, 1e-2, 2, 5, 0, rows=rows)
-    assert_rel_rms(f64(y)[rows], ref, NORM_TOL, "aqn_rmsnorm prefill")
+    assert_rel_rms(f64(y)[rows], ref, NORM_TOL, "aqn_rmsnorm prefill", bf16_out=True)
 
 
 def test_rmsnorm_empty_batch():

@@ -89,4 +89,5 @@ def test_dequantize_exact_and_scaled():
     np.testing.assert_array_equal(exact.double().cpu().numpy(), ref)  # e2m1*e4m3 is exact in bf16
     scaled = q.qerl_nvfp4_dequantize(codes, scales, ts, 40, 96, apply_tensor_scale=True)
     ref_s = oracle.nvfp4_dequantize(oc, osc, ost, 40, 96)
-    np.testing.assert_array_equal(scaled.cpu(), torch.from_numpy(ref_s).float().to(torch.bfloat16))
+    np.testing.assert_array_equal(scaled.float().cpu().numpy(),
+                                  torch.from_numpy(ref_s).float().to(torch.bfloat16).float().numpy())
