@@ -54,8 +54,12 @@ typedef enum {
     QERL_ERR_CUDA = 5,               /* a CUDA runtime call failed */
     QERL_ERR_TIMEOUT = 6,            /* a bounded device-side wait ran out (latched) */
     QERL_ERR_UNSUPPORTED_DEVICE = 7, /* current device is not compute capability 10.3 */
-    QERL_ERR_WORKSPACE = 8           /* workspace missing or smaller than required */
+    QERL_ERR_WORKSPACE = 8,          /* workspace missing or smaller than required */
+    QERL_ERR_TOO_LARGE = 9           /* needs more scratch than the fixed no-allocation buffer */
 } qerl_status;
+
+/* Size of the fixed device scratch buffer behind qerl_nvfp4_lora_linear_fwd_noalloc. */
+#define QERL_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* Block-scale rounding of the quantizer. */
 enum { QERL_SCALE_ROUND_UP = 0, QERL_SCALE_ROUND_NEAREST_EVEN = 1 };
@@ -129,6 +133,33 @@ qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int6
                                        const float *tensor_scale, const void *A, const void *B,
                                        int r, float lora_scale, void *y, float *t_out,
                                        void *ws, size_t ws_bytes, qerl_stream_t stream);
+
+/*
+ * The forward above without a caller-supplied workspace.  The pages have no
+ * counterpart: this is an interface for callers that cannot allocate device
+ * memory -- for example a host framework that owns every device byte through
+ * its own pool and forbids allocations from outside it, or code that must not
+ * call cudaMalloc mid-step because cudaMalloc can synchronize the device.
+ * Computes exactly what qerl_nvfp4_lora_linear_fwd computes (same arguments
+ * minus ws/ws_bytes), using a scratch buffer of QERL_NOALLOC_SCRATCH_BYTES that
+ * lives in the library's own device memory: every GPU that loads the library
+ * holds those bytes until the process exits.
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library call.
+ *   - The first call on a device looks up that buffer's device address (with
+ *     that device current) and caches it; make the first call on each device
+ *     before any stream capture.
+ *   - Shapes whose scratch need, qerl_workspace_bytes(QERL_OP_LINEAR_FWD, M, N,
+ *     K, r), exceeds QERL_NOALLOC_SCRATCH_BYTES return QERL_ERR_TOO_LARGE with
+ *     nothing launched.
+ *   - Every call on a device shares the one buffer: calls whose kernels overlap
+ *     on the GPU (other streams, other host threads) race and corrupt each
+ *     other; serialize them.  The kernels clear what must start at zero.
+ */
+qerl_status qerl_nvfp4_lora_linear_fwd_noalloc(const void *x, int64_t M, int64_t K, int64_t N,
+                                               const uint8_t *codes, const uint8_t *scales,
+                                               const float *tensor_scale, const void *A, const void *B,
+                                               int r, float lora_scale, void *y, float *t_out,
+                                               qerl_stream_t stream);
 
 /*
  * Backward through the frozen NVFP4 weight into the LoRA adapter (bitsofall,

@@ -21,13 +21,15 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libqerl.so")
 QERL_OK = 0
 STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARG", 2: "QERL_ERR_SHAPE", 3: "QERL_ERR_ALIGN",
                 4: "QERL_ERR_NONFINITE", 5: "QERL_ERR_CUDA", 6: "QERL_ERR_TIMEOUT",
-                7: "QERL_ERR_UNSUPPORTED_DEVICE", 8: "QERL_ERR_WORKSPACE"}
+                7: "QERL_ERR_UNSUPPORTED_DEVICE", 8: "QERL_ERR_WORKSPACE", 9: "QERL_ERR_TOO_LARGE"}
+NOALLOC_SCRATCH_BYTES = 8 << 20  # QERL_NOALLOC_SCRATCH_BYTES
 SCALE_ROUND_UP, SCALE_ROUND_NEAREST_EVEN = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_AQN_RMSNORM = 0, 1, 2, 3
 ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
 
 # Every C symbol include/qerl.h declares (checked by the CPU test suite).
 EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_linear_fwd",
+            "qerl_nvfp4_lora_linear_fwd_noalloc",
             "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_noise", "qerl_aqn_sigma",
             "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
             "qerl_launch_count"]
@@ -68,6 +70,8 @@ def lib() -> C.CDLL:
                 "qerl_nvfp4_dequantize": ([vp, vp, vp, i64, i64, vp, i32, vp], i32),
                 "qerl_nvfp4_lora_linear_fwd": ([vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp, vp,
                                                 sz, vp], i32),
+                "qerl_nvfp4_lora_linear_fwd_noalloc": ([vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp,
+                                                        vp], i32),
                 "qerl_nvfp4_lora_linear_bwd": ([vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp,
                                                 vp, vp, i32, vp, sz, vp], i32),
                 "qerl_aqn_rmsnorm": ([vp, i64, i64, vp, f32, f32, u64, u64, u32, vp, vp, sz, vp], i32),
@@ -162,6 +166,19 @@ def qerl_nvfp4_lora_linear_fwd(x, codes, scales, tensor_scale, A, B, lora_scale:
     _check(lib().qerl_nvfp4_lora_linear_fwd(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A), _p(B),
                                             r, float(lora_scale), _p(y), _p(t_out), _p(ws), ws.numel(),
                                             _stream(stream)), "qerl_nvfp4_lora_linear_fwd")
+    return y
+
+
+def qerl_nvfp4_lora_linear_fwd_noalloc(x, codes, scales, tensor_scale, A, B, lora_scale: float, y=None,
+                                       t_out=None, stream=None):
+    """The forward with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/qerl.h)."""
+    M, K = x.shape
+    N, r = B.shape
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(lib().qerl_nvfp4_lora_linear_fwd_noalloc(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A),
+                                                    _p(B), r, float(lora_scale), _p(y), _p(t_out), _stream(stream)),
+           "qerl_nvfp4_lora_linear_fwd_noalloc")
     return y
 
 

@@ -84,6 +84,7 @@ extern "C" const char *qerl_status_string(qerl_status s)
     case QERL_ERR_TIMEOUT: return "bounded device wait timed out";
     case QERL_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (GB300)";
     case QERL_ERR_WORKSPACE: return "workspace missing or too small";
+    case QERL_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation buffer holds";
     }
     return "unknown status";
 }

@@ -208,6 +208,30 @@ size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
     return simt > tc ? simt : tc;
 }
 
+qerl_status linear_fwd_fixed_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
+                                const uint8_t *scales, const float *tensor_scale, const void *A, const void *B, int r,
+                                float lora_scale, void *y, float *t_out, size_t ws_cap,
+                                qerl_status (*get_ws)(void **), cudaStream_t s)
+{
+    QERL_TRY(check_common(M, K, N, codes, scales, tensor_scale, A, B, r));
+    if (M == 0) return QERL_OK;
+    if (!x || !y) return QERL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || (t_out && !aligned16(t_out))) return QERL_ERR_ALIGN;
+    const size_t need = linear_fwd_ws_bytes(M, N, K, r);
+    if (need > ws_cap) return QERL_ERR_TOO_LARGE;
+    QERL_TRY(check_device());
+    void *ws = nullptr;
+    QERL_TRY(get_ws(&ws));
+    const FwdArgs a{static_cast<const __nv_bfloat16 *>(x), M, K, N, codes, scales, tensor_scale,
+                    static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), r,
+                    lora_scale, static_cast<__nv_bfloat16 *>(y), t_out};
+    if (g_algo.load() != QERL_ALGO_SIMT) {
+        const qerl_status st = tc_linear_fwd(a, static_cast<char *>(ws), ws_cap, s);
+        if (st != QERL_ERR_SHAPE) return st;
+    }
+    return simt_fwd(a, static_cast<char *>(ws), s);
+}
+
 }  // namespace qerl
 
 using namespace qerl;

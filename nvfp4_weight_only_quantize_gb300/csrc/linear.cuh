@@ -44,4 +44,12 @@ qerl_status tc_linear_bwd(const BwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
 
 inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// Forward with a fixed scratch buffer: validates the arguments like the
+// workspace entry point, returns QERL_ERR_TOO_LARGE when the call needs more
+// than ws_cap bytes, then asks get_ws for the buffer and runs the same kernels.
+qerl_status linear_fwd_fixed_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
+                                const uint8_t *scales, const float *tensor_scale, const void *A, const void *B, int r,
+                                float lora_scale, void *y, float *t_out, size_t ws_cap,
+                                qerl_status (*get_ws)(void **), cudaStream_t s);
+
 }  // namespace qerl
