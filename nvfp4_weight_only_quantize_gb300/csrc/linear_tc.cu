@@ -11,12 +11,14 @@
 // numbers and ysc is finite (see tc_exponent_offset).
 //
 // Warp roles (352 threads, one CTA per SM):
-//   warps 0-7  dequantize: packed codes (smem) + scales (global) -> bf16 A tile
-//              in the 128-byte-swizzled K-major layout; warps 0-3 also run the
-//              epilogue (TMEM -> registers -> y, or split-K partials).
-//   warp 8     TMA producer of the packed codes (deep ring, streamed once).
-//   warp 9     TMA producer of the token tile (x, then u for the LoRA steps).
-//   warp 10    allocates TMEM; lane 0 issues tcgen05.mma and the commits.
+//   warps 0-15 dequantize, as four groups of four warps taking every fourth k-step:
+//              packed codes + block scales (smem) -> bf16 A tile in the
+//              128-byte-swizzled K-major layout; warps 0-3 also run the
+//              epilogue (TMEM -> registers -> smem -> y, or split-K partials).
+//   warp 16    TMA producer of the packed codes and block scales, 4 k-steps
+//              (256 k: 128 code bytes per row, full lines) per raw stage.
+//   warp 17    TMA producer of the token tile (x, then u for the LoRA steps).
+//   warp 18    allocates TMEM; lane 0 issues tcgen05.mma and the commits.
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA latches
 // QERL_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
 // drained (bounded), TMEM is freed and the CTA exits.
@@ -34,23 +36,37 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BK = 64;          // k per stage: one 128-byte swizzle row of bf16
+constexpr int BK = 64;          // k per MMA step: one 128-byte swizzle row of bf16
+constexpr int GK = 4;           // k-steps per raw stage (256 k)
 constexpr int TILE_N = 128;     // weight rows per CTA (MMA M)
-constexpr int NUM_DQ_WARPS = 8;
-constexpr int WARP_RAW = 8, WARP_X = 9, WARP_MMA = 10;
-constexpr int NUM_THREADS = 11 * 32;
-constexpr int RAW_STAGE = 4096;  // 128 rows x 32 code bytes, stored as [2][128][16]
-constexpr int A_BYTES = TILE_N * BK * 2;
+constexpr int DQ_GROUPS = 4;      // dequant groups; group g takes the k-steps i = g (mod DQ_GROUPS)
+constexpr int DQ_GROUP_WARPS = 4; // one warp per 32 weight rows of the tile
+constexpr int NUM_DQ_WARPS = DQ_GROUPS * DQ_GROUP_WARPS;
+constexpr int WARP_RAW = NUM_DQ_WARPS, WARP_X = NUM_DQ_WARPS + 1, WARP_MMA = NUM_DQ_WARPS + 2;
+constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
+constexpr int RAW_CODES = TILE_N * GK * BK / 2;    // 16 KB: 128 rows x 128 code bytes (SW128)
+constexpr int RAW_SCALES = TILE_N * GK * BK / 16;  // 2 KB: 128 rows x 16 scale bytes
+constexpr int RAW_STAGE = RAW_CODES + RAW_SCALES;  // 18 KB, a multiple of 1024
+constexpr int MAX_SPLITS = 8;  // split-K factor cap: bounds the fixup's partial reads
 
 template <int BN>
 struct Cfg {
-    static constexpr int S = BN >= 256 ? 3 : 4;                         // dequantized A-tile stages
-    static constexpr int XS = BN >= 256 ? 3 : (BN >= 128 ? 4 : 8);      // token-tile stages
-    static constexpr int R = BN >= 128 ? 8 : (BN >= 64 ? 12 : 16);      // packed-code stages
+    // Stages of the dequantized A tile (TMEM) and of the token tile (smem) go in
+    // lockstep: one MMA commit per k-step frees both.  At least DQ_GROUPS: a group
+    // may then never wait on a stage two mbarrier phases ahead (parity aliasing).
+    static constexpr int S = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    static_assert(S >= DQ_GROUPS, "parity waits need at least one stage per dequant group");
+    static constexpr int R = BN >= 256 ? 4 : (BN >= 128 ? 5 : (BN >= 64 ? 6 : 8));  // raw (code+scale) stages
     static constexpr int X_BYTES = BN * BK * 2;
-    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+    // TMEM: the f32 accumulator (BN columns), then S A stages of 32 columns
+    // (128 rows x 64 bf16, two per 32-bit column).
+    static constexpr int A_COL0 = BN < 32 ? 32 : BN;
+    static constexpr int TMEM_NEED = A_COL0 + S * 32;
+    static constexpr int TMEM_COLS = TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512));
+    static_assert(TMEM_NEED <= 512, "TMEM holds 512 columns");
     static constexpr int BAR_BYTES = 1024;
-    static constexpr int SMEM = S * A_BYTES + XS * X_BYTES + R * RAW_STAGE + BAR_BYTES + 1024;
+    static constexpr int SMEM = S * X_BYTES + R * RAW_STAGE + BAR_BYTES + 1024;
+    static_assert(S * X_BYTES >= BN * TILE_N * 2, "the y staging tile reuses the token ring");
 };
 
 struct TcFwdParams {
@@ -109,65 +125,73 @@ __device__ __forceinline__ void dequant_word(uint32_t q, uint32_t f2, uint32_t *
     }
 }
 
-__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p)
+// 16 columns of this warp's 32 TMEM lanes of the accumulator, as floats.
+__device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
 {
-    uint16_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
-    return v;
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap x_map,
-                  const __grid_constant__ CUtensorMap u_map, const TcFwdParams p)
+                  const __grid_constant__ CUtensorMap u_map, const __grid_constant__ CUtensorMap scl_map,
+                  const TcFwdParams p)
 {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *A_ring = smem;
-    uint8_t *X_ring = A_ring + C::S * A_BYTES;
-    uint8_t *R_ring = X_ring + C::XS * C::X_BYTES;
+    uint8_t *X_ring = smem;
+    uint8_t *R_ring = X_ring + C::S * C::X_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(R_ring + C::R * RAW_STAGE);
     uint64_t *raw_full = bars;
     uint64_t *raw_empty = raw_full + C::R;
     uint64_t *x_full = raw_empty + C::R;
-    uint64_t *x_empty = x_full + C::XS;
-    uint64_t *a_full = x_empty + C::XS;
-    uint64_t *a_empty = a_full + C::S;
-    uint64_t *acc_full = a_empty + C::S;
+    uint64_t *a_full = x_full + C::S;
+    uint64_t *stage_empty = a_full + C::S;  // MMA of the stage done: frees its A and token tiles
+    uint64_t *acc_full = stage_empty + C::S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
+    volatile int *ep_ok = last_flag + 1;  // [4]: epilogue warps' view of acc_full
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x % p.splits;
     const int tile = blockIdx.x / p.splits;
     const int n_tile = tile % p.n_tiles, m_tile = tile / p.n_tiles;
     const int n0 = n_tile * TILE_N, m0 = m_tile * BN;
-    const int k_begin = split * p.steps_per_split;
+    const int k_begin = split * p.steps_per_split;  // a multiple of GK
     const int k_end = min(p.nk, k_begin + p.steps_per_split);
     const int n_main = k_end > k_begin ? k_end - k_begin : 0;
+    const int n_groups = (n_main + GK - 1) / GK;  // n_main is a multiple of GK (K % 256 == 0)
     const int n_steps = n_main + (split == p.splits - 1 ? p.lora_steps : 0);
+    // Every CTA walks its k-range from a different raw group, so that the CTAs
+    // do not all read the same token tile from L2 at the same time.
+    const int grot = n_groups > 0 ? (n_tile * 5 + m_tile * 3) % n_groups : 0;
+    auto kstep = [&](int i) { return k_begin + ((i / GK + grot) % n_groups) * GK + i % GK; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::R; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], NUM_DQ_WARPS);
         }
-        for (int i = 0; i < C::XS; ++i) {
-            mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], 1);
-        }
         for (int i = 0; i < C::S; ++i) {
-            mbar_init(&a_full[i], NUM_DQ_WARPS);
-            mbar_init(&a_empty[i], 1);
+            mbar_init(&x_full[i], 1);
+            mbar_init(&a_full[i], DQ_GROUP_WARPS);
+            mbar_init(&stage_empty[i], 1);
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
     }
-    if (warp == WARP_RAW && lane == 0) prefetch_tensormap(&codes_map);
+    if (warp == WARP_RAW && lane == 0) {
+        prefetch_tensormap(&codes_map);
+        prefetch_tensormap(&scl_map);
+    }
     if (warp == WARP_X && lane == 0) {
         prefetch_tensormap(&x_map);
         prefetch_tensormap(&u_map);
@@ -183,10 +207,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const unsigned long long deadline = globaltimer_ns() + p.timeout_ns;
 
     // Bounded wait for the phase with this parity; false once the CTA aborts.
+    // Waiting threads poll with a short sleep between tries rather than
+    // spinning: the dequantizing warps are issue-bound, and a spinning waiter
+    // (a role thread, or the dequant group whose turn it is not) takes their
+    // scheduler slots.
+    const unsigned sleep_ns = warp >= NUM_DQ_WARPS ? 64u : 32u;
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         if (mbar_try_wait(bar, parity)) return true;
         for (;;) {
             if (*abort_flag) return false;
+            __nanosleep(sleep_ns);
             if (mbar_try_wait(bar, parity)) return true;
             if (globaltimer_ns() > deadline) {
                 *abort_flag = 1;
@@ -203,106 +233,126 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
 
     if (warp == WARP_RAW) {
-        // ---------------------------------------------------------- packed codes
+        // ------------------------------------------- packed codes + block scales
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int issued = 0;
-            for (int i = 0; i < n_main; ++i) {
-                const int slot = i % C::R;
-                const uint32_t round = (uint32_t)(i / C::R);
+            for (int g = 0; g < n_groups; ++g) {
+                const int slot = g % C::R;
+                const uint32_t round = (uint32_t)(g / C::R);
                 if (round > 0 && !wait(&raw_empty[slot], (round - 1) & 1u)) break;
                 mbar_arrive_expect_tx(&raw_full[slot], RAW_STAGE);
-                const int kb = (k_begin + i) * (BK / 2);
+                const int kk = kstep(g * GK);  // first k-step of the group
                 uint8_t *dst = R_ring + slot * RAW_STAGE;
-                tma_load_2d_hint(dst, &codes_map, &raw_full[slot], kb, n0, pol);
-                tma_load_2d_hint(dst + 2048, &codes_map, &raw_full[slot], kb + 16, n0, pol);
-                issued = i + 1;
+                tma_load_2d_hint(dst, &codes_map, &raw_full[slot], kk * (BK / 2), n0, pol);
+                tma_load_2d_hint(dst + RAW_CODES, &scl_map, &raw_full[slot], kk * (BK / 16), n0, pol);
+                issued = g + 1;
             }
             if (*abort_flag)  // let the copies already issued land before the CTA exits
-                for (int i = issued > C::R ? issued - C::R : 0; i < issued; ++i)
-                    drain_wait(&raw_full[i % C::R], (uint32_t)(i / C::R) & 1u);
+                for (int g = issued > C::R ? issued - C::R : 0; g < issued; ++g)
+                    drain_wait(&raw_full[g % C::R], (uint32_t)(g / C::R) & 1u);
         }
         __syncwarp();
     } else if (warp == WARP_X) {
-        // ---------------------------------------------------------- token tiles
+        // ------------------------------------------- token tiles
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
-            // The token tiles (and u) may be written by the kernel launched just
-            // before this one: wait for it here (no-op without a programmatic
-            // launch dependency).  Weights are static and are streamed before it.
-            asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
             for (int i = 0; i < n_steps; ++i) {
-                const int slot = i % C::XS;
-                const uint32_t round = (uint32_t)(i / C::XS);
-                if (round > 0 && !wait(&x_empty[slot], (round - 1) & 1u)) break;
+                const int slot = i % C::S;
+                const uint32_t round = (uint32_t)(i / C::S);
+                // u is written by the LoRA down-projection launched just before
+                // this kernel, which lets this grid start early (programmatic
+                // launch): wait for that grid only before the first u tile.  The
+                // token tiles x were complete before that grid was launched.
+                if (i == n_main) asm volatile("griddepcontrol.wait;" ::: "memory");
+                if (round > 0 && !wait(&stage_empty[slot], (round - 1) & 1u)) break;
                 mbar_arrive_expect_tx(&x_full[slot], C::X_BYTES);
                 uint8_t *dst = X_ring + slot * C::X_BYTES;
                 if (i < n_main)
-                    tma_load_2d_hint(dst, &x_map, &x_full[slot], (k_begin + i) * BK, m0, pol);
+                    tma_load_2d_hint(dst, &x_map, &x_full[slot], kstep(i) * BK, m0, pol);
                 else
                     tma_load_2d_hint(dst, &u_map, &x_full[slot], (i - n_main) * BK, m0, pol);
                 issued = i + 1;
             }
             if (*abort_flag)
-                for (int i = issued > C::XS ? issued - C::XS : 0; i < issued; ++i)
-                    drain_wait(&x_full[i % C::XS], (uint32_t)(i / C::XS) & 1u);
+                for (int i = issued > C::S ? issued - C::S : 0; i < issued; ++i)
+                    drain_wait(&x_full[i % C::S], (uint32_t)(i / C::S) & 1u);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
-        // ---------------------------------------------------------- MMA issue
+        // ------------------------------------------- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(TILE_N, BN);
-            for (int i = 0; i < n_steps; ++i) {
-                const int s = i % C::S, xs = i % C::XS;
-                if (!wait(&a_full[s], (uint32_t)(i / C::S) & 1u) || !wait(&x_full[xs], (uint32_t)(i / C::XS) & 1u))
-                    break;
+            // An mbarrier query costs the issuing thread ~80 cycles of latency, as
+            // long as four small MMAs: the next step's barriers are probed before
+            // this step's MMAs are issued, and waited on only if the probe failed.
+            bool ready = n_steps > 0 && wait(&a_full[0], 0) && wait(&x_full[0], 0);
+            for (int i = 0; i < n_steps && ready; ++i) {
+                const int s = i % C::S;
+                const int s1 = (i + 1) % C::S;
+                const uint32_t par1 = (uint32_t)((i + 1) / C::S) & 1u;
+                const bool more = i + 1 < n_steps;
+                const bool pa = more && mbar_try_wait(&a_full[s1], par1);
+                const bool px = more && mbar_try_wait(&x_full[s1], par1);
                 tc_fence_after();
-                const uint64_t ad = desc_kmajor_sw128(smem_u32(A_ring + s * A_BYTES));
-                const uint64_t bd = desc_kmajor_sw128(smem_u32(X_ring + xs * C::X_BYTES));
+                const uint32_t at = tmem + (uint32_t)(C::A_COL0 + s * 32);
+                const uint64_t bd = desc_kmajor_sw128(smem_u32(X_ring + s * C::X_BYTES));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    umma_bf16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&a_empty[s]);
-                umma_commit(&x_empty[xs]);
+                for (int kk = 0; kk < BK / 16; ++kk)  // 16 k = 8 TMEM columns of A
+                    umma_bf16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&stage_empty[s]);
+                if (more) ready = (pa || wait(&a_full[s1], par1)) && (px || wait(&x_full[s1], par1));
             }
             // Arrives once every MMA issued above has completed (also after an abort).
             umma_commit(acc_full);
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------------- dequantize
+        // ------------------------------------------- dequantize
+        // Group g = warp / 4 takes the steps i = g, g + DQ_GROUPS, ...; thread =
+        // one weight row of the tile, all 64 k of the step (32 code bytes).
         const int row = (warp & 3) * 32 + lane;
-        const int khalf = warp >> 2;
+        const int group = warp >> 2;
         const int n = n0 + row;
         const bool row_ok = n < p.N;
-        const uint8_t *srow = p.scales + (size_t)(row_ok ? n : 0) * (size_t)(p.K / 16) + 2 * khalf;
         const float pow2 = pow2f(126 - tc_exponent_offset(*p.tensor_scale));
-        const uint32_t a_row = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
-        uint32_t sc_next = (row_ok && n_main > 0) ? ldg_u16(srow + (size_t)k_begin * 4) : 0u;
-        for (int i = 0; i < n_steps; ++i) {
-            uint32_t out[16];
+        for (int i = group; i < n_steps; i += DQ_GROUPS) {
+            uint32_t out[32];
             if (i < n_main) {
-                const int rs = i % C::R;
-                if (!__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(i / C::R) & 1u))) break;
-                const uint4 c = ld_shared_v4(smem_u32(R_ring + rs * RAW_STAGE + khalf * 2048 + row * 16));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[rs]);
-                const uint32_t sc = sc_next;
-                if (row_ok && i + 1 < n_main) sc_next = ldg_u16(srow + (size_t)(k_begin + i + 1) * 4);
+                const int g = i / GK, rs = g % C::R, q = i % GK;
+                const bool first_in_stage = q < DQ_GROUPS;  // this group's first step of the raw stage
+                if (first_in_stage && !__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(g / C::R) & 1u))) break;
+                // codes: row `row`, logical 16-byte chunks 2q and 2q+1 of the 128-byte
+                // row, stored by TMA at chunk ^ (row % 8)
+                const uint32_t rb = smem_u32(R_ring + rs * RAW_STAGE) + row * 128;
+                const uint4 c0 = ld_shared_v4(rb + (uint32_t)(((2 * q) ^ (row & 7)) * 16));
+                const uint4 c1 = ld_shared_v4(rb + (uint32_t)(((2 * q + 1) ^ (row & 7)) * 16));
+                const uint32_t sc =
+                    *reinterpret_cast<const uint32_t *>(R_ring + rs * RAW_STAGE + RAW_CODES + row * 16 + q * 4);
+                if (q >= GK - DQ_GROUPS || i + DQ_GROUPS >= n_main) {  // this group's last step of the raw stage
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&raw_empty[rs]);
+                }
                 const uint32_t f0 = scale_factor_bf16x2(sc & 0xFFu, pow2);
-                const uint32_t f1 = scale_factor_bf16x2(sc >> 8, pow2);
-                dequant_word(c.x, f0, out + 0);
-                dequant_word(c.y, f0, out + 4);
-                dequant_word(c.z, f1, out + 8);
-                dequant_word(c.w, f1, out + 12);
+                const uint32_t f1 = scale_factor_bf16x2((sc >> 8) & 0xFFu, pow2);
+                const uint32_t f2 = scale_factor_bf16x2((sc >> 16) & 0xFFu, pow2);
+                const uint32_t f3 = scale_factor_bf16x2(sc >> 24, pow2);
+                dequant_word(c0.x, f0, out + 0);
+                dequant_word(c0.y, f0, out + 4);
+                dequant_word(c0.z, f1, out + 8);
+                dequant_word(c0.w, f1, out + 12);
+                dequant_word(c1.x, f2, out + 16);
+                dequant_word(c1.y, f2, out + 20);
+                dequant_word(c1.z, f3, out + 24);
+                dequant_word(c1.w, f3, out + 28);
             } else {
-                // LoRA up-projection rows: B[n, l*64 + khalf*32 .. +31], zero past r.
-                const int j0 = (i - n_main) * BK + khalf * 32;
+                // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
+                const int j0 = (i - n_main) * BK;
                 const __nv_bfloat16 *b = p.Bl + (size_t)(row_ok ? n : 0) * p.r + j0;
-                if (row_ok && (p.r & 7) == 0 && j0 + 32 <= p.r) {
+                if (row_ok && (p.r & 7) == 0 && j0 + 64 <= p.r) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 8; ++q) {
                         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(b) + q);
                         out[4 * q] = v.x;
                         out[4 * q + 1] = v.y;
@@ -312,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 } else {
                     const uint16_t *bh = reinterpret_cast<const uint16_t *>(b);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                    for (int q = 0; q < 32; ++q) {
                         const uint32_t lo = (row_ok && j0 + 2 * q < p.r) ? bh[2 * q] : 0u;
                         const uint32_t hi = (row_ok && j0 + 2 * q + 1 < p.r) ? bh[2 * q + 1] : 0u;
                         out[q] = lo | (hi << 16);
@@ -321,48 +371,60 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const int s = i % C::S;
             const uint32_t sround = (uint32_t)(i / C::S);
-            if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&a_empty[s], (sround - 1) & 1u))) break;
-            const uint32_t abase = smem_u32(A_ring + s * A_BYTES) + a_row;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t phys = (uint32_t)((khalf * 4 + q) ^ (row & 7));
-                st_shared_v4(abase + phys * 16, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-            }
-            fence_proxy_async_smem();
+            if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&stage_empty[s], (sround - 1) & 1u))) break;
+            // row `row` of the A stage: TMEM lane `row`, 32 columns of bf16 pairs
+            tmem_st32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(C::A_COL0 + s * 32), out);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
             const bool withhold = p.fault && blockIdx.x == 0 && warp == 0 && i == 0;
             if (lane == 0 && !withhold) mbar_arrive(&a_full[s]);
         }
 
-        // ---------------------------------------------------------- epilogue
+        // ------------------------------------------- epilogue (warps 0-3)
         if (warp < 4) {
-            const bool ok = __all_sync(0xFFFFFFFFu, wait(acc_full, 0));
+            const bool ok_warp = __all_sync(0xFFFFFFFFu, wait(acc_full, 0));
+            if (lane == 0) ep_ok[warp] = ok_warp ? 1 : 0;
+            named_bar_sync(1, 128);  // one decision for all four epilogue warps
+            const bool ok = ep_ok[0] && ep_ok[1] && ep_ok[2] && ep_ok[3];
             tc_fence_after();
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // the workspace and y follow the predecessor
             if (ok) {
                 const float st = *p.tensor_scale;
                 const float ysc = st * pow2f(tc_exponent_offset(st));
                 const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
                 if (p.splits == 1) {
+                    // TMEM -> bf16 tile Y[token][row] in the (now idle) token ring,
+                    // then 16-byte row-contiguous stores to y.
+                    uint8_t *Y = X_ring;
                     for (int c0 = 0; c0 < BN; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(taddr + (uint32_t)c0, v);
-                        tmem_wait_ld();
-                        if (row_ok) {
+                        float v[16];
+                        acc_load16(taddr + (uint32_t)c0, v);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int m = m0 + c0 + j;
-                                if (m < p.M) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(__uint_as_float(v[j]) * ysc);
-                            }
+                        for (int j = 0; j < 16; ++j)
+                            reinterpret_cast<__nv_bfloat16 *>(Y)[(c0 + j) * TILE_N + row] = __float2bfloat16_rn(v[j] * ysc);
+                    }
+                    named_bar_sync(1, 128);
+                    const bool vec = (p.N % 8) == 0;
+                    for (int v = threadIdx.x; v < BN * (TILE_N / 8); v += 128) {
+                        const int m = m0 + v / (TILE_N / 8), nn = n0 + (v % (TILE_N / 8)) * 8;
+                        if (m >= p.M || nn >= p.N) continue;
+                        const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(Y) +
+                                                   (v / (TILE_N / 8)) * TILE_N + (v % (TILE_N / 8)) * 8;
+                        __nv_bfloat16 *dst = p.y + (size_t)m * p.N + nn;
+                        if (vec && nn + 8 <= p.N) {
+                            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+                        } else {
+                            for (int e = 0; e < 8 && nn + e < p.N; ++e) dst[e] = src[e];
                         }
                     }
                 } else {
                     float *part = p.partial + ((size_t)tile * p.splits + split) * (size_t)(TILE_N * BN);
                     for (int c0 = 0; c0 < BN; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(taddr + (uint32_t)c0, v);
-                        tmem_wait_ld();
+                        float v[16];
+                        acc_load16(taddr + (uint32_t)c0, v);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * TILE_N + row, __uint_as_float(v[j]));
+                        for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * TILE_N + row, v[j]);
                     }
                     __threadfence();
                     named_bar_sync(1, 128);
@@ -384,25 +446,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float st = *p.tensor_scale;
         const float ysc = st * pow2f(tc_exponent_offset(st));
         const float *base = p.partial + (size_t)tile * p.splits * (size_t)(TILE_N * BN);
-        for (int it = threadIdx.x; it < BN * (TILE_N / 4); it += NUM_THREADS) {
-            const int col = it / (TILE_N / 4), rq = (it % (TILE_N / 4)) * 4;
-            const int m = m0 + col;
-            if (m >= p.M) continue;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int s2 = 0; s2 < p.splits; ++s2) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN) +
-                                                                         (size_t)col * TILE_N + rq));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        constexpr int ITEMS = BN * (TILE_N / 4);
+        for (int it0 = threadIdx.x; it0 < ITEMS; it0 += 2 * NUM_THREADS) {
+            float4 v[2][MAX_SPLITS];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int n = n0 + rq + e;
-                if (n < p.N) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(a4[e] * ysc);
+            for (int h = 0; h < 2; ++h) {
+                const int it = it0 + h * NUM_THREADS;
+                const int col = it / (TILE_N / 4), rq = (it % (TILE_N / 4)) * 4;
+#pragma unroll
+                for (int s2 = 0; s2 < MAX_SPLITS; ++s2)
+                    v[h][s2] = (it < ITEMS && s2 < p.splits)
+                                   ? __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN) +
+                                                                            (size_t)col * TILE_N + rq))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int it = it0 + h * NUM_THREADS;
+                if (it >= ITEMS) break;
+                const int col = it / (TILE_N / 4), rq = (it % (TILE_N / 4)) * 4;
+                const int m = m0 + col;
+                if (m >= p.M) continue;
+                float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s2 = 0; s2 < MAX_SPLITS; ++s2) {  // fixed split order
+                    a4[0] += v[h][s2].x;
+                    a4[1] += v[h][s2].y;
+                    a4[2] += v[h][s2].z;
+                    a4[3] += v[h][s2].w;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int n = n0 + rq + e;
+                    if (n < p.N) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(a4[e] * ysc);
+                }
             }
         }
         if (threadIdx.x == 0) p.counters[tile] = 0u;
@@ -553,11 +630,12 @@ FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
     if (tiles < sms) {
         splits = (int)(sms / tiles);
         int max_splits = pl.nk / 2 > 0 ? pl.nk / 2 : 1;  // at least two k-steps per split
-        if (max_splits > 16) max_splits = 16;          // bounds the fixup's partial traffic
+        if (max_splits > MAX_SPLITS) max_splits = MAX_SPLITS;
         if (splits > max_splits) splits = max_splits;
         if (splits < 1) splits = 1;
     }
     pl.sps = (pl.nk + splits - 1) / splits;
+    pl.sps = (pl.sps + GK - 1) / GK * GK;  // splits start on a raw-stage boundary
     pl.splits = (pl.nk + pl.sps - 1) / pl.sps;  // no empty split
     pl.off_u = 0;
     pl.off_cnt = round256(size_t(M) * pl.r_pad * 2);
@@ -568,7 +646,8 @@ FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
 
 bool tc_fwd_applies(int64_t M, int64_t N, int64_t K, int r)
 {
-    return M >= 1 && N >= 1 && K >= BK && K % BK == 0 && r >= 1 && r <= 256 && M <= (1 << 30) &&
+    // K % 256: the scale rows (K/16 bytes) must be a multiple of 16 bytes for TMA
+    return M >= 1 && N >= 1 && K >= GK * BK && K % (GK * BK) == 0 && r >= 1 && r <= 256 && M <= (1 << 30) &&
            N <= (1 << 30) && K <= (1 << 30);
 }
 
@@ -591,8 +670,8 @@ const Env &env()
 }
 
 template <int BN>
-qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const TcFwdParams &p,
-                       unsigned grid, cudaStream_t s)
+qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const CUtensorMap &sm,
+                       const TcFwdParams &p, unsigned grid, cudaStream_t s)
 {
     if (cudaFuncSetAttribute(tc_fwd_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) !=
         cudaSuccess)
@@ -610,7 +689,7 @@ qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUten
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, tc_fwd_kernel<BN>, cm, xm, um, p) != cudaSuccess) return QERL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, tc_fwd_kernel<BN>, cm, xm, um, sm, p) != cudaSuccess) return QERL_ERR_CUDA;
     return launched();
 }
 
@@ -633,8 +712,12 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     float *partial = reinterpret_cast<float *>(ws + pl.off_part);
     const int tiles = pl.n_tiles * pl.m_tiles;
 
-    CUtensorMap cm, xm, um;
-    if (!make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, a.K / 2, a.N, a.K / 2, 16, TILE_N,
+    CUtensorMap cm, xm, um, sm;
+    // codes: 128 rows x 128 bytes (4 k-steps) per box, 128-byte swizzle; scales:
+    // 128 rows x 16 bytes (the same 4 k-steps); token tiles: BN rows x 64 bf16.
+    if (!make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, a.K / 2, a.N, a.K / 2, GK * BK / 2, TILE_N,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&sm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, a.K / 16, a.N, a.K / 16, GK * BK / 16, TILE_N,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, a.K * 2, BK, pl.BN,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -644,11 +727,19 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
 
     // 1) LoRA down-projection (+ counter reset)
     {
-        constexpr int MB = 8, JB = 4;
-        const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
-        lora_down_kernel<MB, JB><<<blocks, LD_THREADS, 0, s>>>(a.x, a.A, (int)a.M, (int)a.K, a.r, pl.r_pad,
-                                                               a.lora_scale, a.tensor_scale, a.t_out, u, counters,
-                                                               tiles);
+        if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
+            constexpr int MB = 4, JB = 2;
+            const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
+            lora_down_kernel<MB, JB><<<blocks, LD_THREADS, 0, s>>>(a.x, a.A, (int)a.M, (int)a.K, a.r, pl.r_pad,
+                                                                   a.lora_scale, a.tensor_scale, a.t_out, u,
+                                                                   counters, tiles);
+        } else {
+            constexpr int MB = 8, JB = 4;
+            const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
+            lora_down_kernel<MB, JB><<<blocks, LD_THREADS, 0, s>>>(a.x, a.A, (int)a.M, (int)a.K, a.r, pl.r_pad,
+                                                                   a.lora_scale, a.tensor_scale, a.t_out, u,
+                                                                   counters, tiles);
+        }
         QERL_TRY(launched());
     }
 
@@ -676,11 +767,11 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     p.fault = env().fault;
     const unsigned grid = (unsigned)(tiles * pl.splits);
     switch (pl.BN) {
-    case 16: return launch_fwd<16>(cm, xm, um, p, grid, s);
-    case 32: return launch_fwd<32>(cm, xm, um, p, grid, s);
-    case 64: return launch_fwd<64>(cm, xm, um, p, grid, s);
-    case 128: return launch_fwd<128>(cm, xm, um, p, grid, s);
-    default: return launch_fwd<256>(cm, xm, um, p, grid, s);
+    case 16: return launch_fwd<16>(cm, xm, um, sm, p, grid, s);
+    case 32: return launch_fwd<32>(cm, xm, um, sm, p, grid, s);
+    case 64: return launch_fwd<64>(cm, xm, um, sm, p, grid, s);
+    case 128: return launch_fwd<128>(cm, xm, um, sm, p, grid, s);
+    default: return launch_fwd<256>(cm, xm, um, sm, p, grid, s);
     }
 }
 
