@@ -11,14 +11,18 @@
 // numbers and ysc is finite (see tc_exponent_offset).
 //
 // Warp roles (352 threads, one CTA per SM):
-//   warps 0-15 dequantize, as four groups of four warps taking every fourth k-step:
+//   warps 0-7  dequantize, as two groups of four warps taking alternate stages:
 //              packed codes + block scales (smem) -> bf16 A tile in the
 //              128-byte-swizzled K-major layout; warps 0-3 also run the
 //              epilogue (TMEM -> registers -> smem -> y, or split-K partials).
-//   warp 16    TMA producer of the packed codes and block scales, 4 k-steps
+//   warp 8     TMA producer of the packed codes and block scales, 4 k-steps
 //              (256 k: 128 code bytes per row, full lines) per raw stage.
-//   warp 17    TMA producer of the token tile (x, then u for the LoRA steps).
-//   warp 18    allocates TMEM; lane 0 issues tcgen05.mma and the commits.
+//   warp 9     TMA producer of the token tile (x, then u for the LoRA steps).
+//   warp 10    allocates TMEM and issues tcgen05.mma and the commits (one
+//              elected lane of the converged warp).
+// A pipeline stage is SPS k-steps: 4 (one raw stage) for token tiles up to 128,
+// 2 for 256-token tiles (their token stages are larger); each stage costs every
+// role mbarrier round trips of ~100+ cycles, so stages are made long.
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA latches
 // QERL_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
 // drained (bounded), TMEM is freed and the CTA exits.
@@ -39,9 +43,10 @@ using namespace ptx;
 constexpr int BK = 64;          // k per MMA step: one 128-byte swizzle row of bf16
 constexpr int GK = 4;           // k-steps per raw stage (256 k)
 constexpr int TILE_N = 128;     // weight rows per CTA (MMA M)
-constexpr int DQ_GROUPS = 4;      // dequant groups; group g takes the k-steps i = g (mod DQ_GROUPS)
+constexpr int DQ_GROUPS = 2;      // dequant groups; group g takes the stages j = g (mod DQ_GROUPS)
 constexpr int DQ_GROUP_WARPS = 4; // one warp per 32 weight rows of the tile
 constexpr int NUM_DQ_WARPS = DQ_GROUPS * DQ_GROUP_WARPS;
+static_assert(DQ_GROUPS == 2, "the epilogue and TMEM budget assume two dequant groups");
 constexpr int WARP_RAW = NUM_DQ_WARPS, WARP_X = NUM_DQ_WARPS + 1, WARP_MMA = NUM_DQ_WARPS + 2;
 constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
 constexpr int RAW_CODES = TILE_N * GK * BK / 2;    // 16 KB: 128 rows x 128 code bytes (SW128)
@@ -51,22 +56,36 @@ constexpr int MAX_SPLITS = 8;  // split-K factor cap: bounds the fixup's partial
 
 template <int BN>
 struct Cfg {
-    // Stages of the dequantized A tile (TMEM) and of the token tile (smem) go in
-    // lockstep: one MMA commit per k-step frees both.  At least DQ_GROUPS: a group
-    // may then never wait on a stage two mbarrier phases ahead (parity aliasing).
-    static constexpr int S = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    // k-steps per pipeline stage: every stage costs the MMA issuer one barrier
+    // round trip and one commit, so small token tiles (short MMAs) take two.
+    static constexpr int SPS = BN >= 256 ? 2 : 4;
+    // A stage holds SPS k-steps of the dequantized weight tile (TMEM); at least
+    // DQ_GROUPS of them, so a group never waits on a stage two mbarrier phases
+    // ahead of the MMA (parity aliasing).
+    // A stages (TMEM); a power of two: slot and phase are a mask and a shift.
+    static constexpr int S = SPS == 4 ? 2 : 4;
+    static constexpr int LOG_S = SPS == 4 ? 1 : 2;
     static_assert(S >= DQ_GROUPS, "parity waits need at least one stage per dequant group");
-    static constexpr int R = BN >= 256 ? 4 : (BN >= 128 ? 5 : (BN >= 64 ? 6 : 8));  // raw (code+scale) stages
-    static constexpr int X_BYTES = BN * BK * 2;
-    // TMEM: the f32 accumulator (BN columns), then S A stages of 32 columns
-    // (128 rows x 64 bf16, two per 32-bit column).
+    // Token-tile stages (smem), deeper than the A ring: a token slot is reloaded
+    // only after the MMA that read it completed, a ~2 us round trip.
+    static constexpr int XS = BN >= 128 ? 2 : 4;
+    static constexpr int LOG_XS = BN >= 128 ? 1 : 2;
+    static constexpr int R = 4;  // raw (code+scale) stages
+    static_assert(GK % SPS == 0 && GK / SPS <= DQ_GROUPS, "each group has at most one stage per raw stage");
+    static_assert((1 << LOG_S) == S && (1 << LOG_XS) == XS, "power-of-two rings");
+    static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
+    static_assert(R * GK >= S * SPS, "raw ring deep enough for parity-safe waits");
+    static constexpr int X_STEP = BN * BK * 2;
+    static constexpr int X_STAGE = X_STEP * SPS;
+    // TMEM: the f32 accumulator (BN columns), then S A stages of 32*SPS columns
+    // (128 rows x 64 bf16 per step, two per 32-bit column).
     static constexpr int A_COL0 = BN < 32 ? 32 : BN;
-    static constexpr int TMEM_NEED = A_COL0 + S * 32;
+    static constexpr int TMEM_NEED = A_COL0 + S * 32 * SPS;
     static constexpr int TMEM_COLS = TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512));
     static_assert(TMEM_NEED <= 512, "TMEM holds 512 columns");
     static constexpr int BAR_BYTES = 1024;
-    static constexpr int SMEM = S * X_BYTES + R * RAW_STAGE + BAR_BYTES + 1024;
-    static_assert(S * X_BYTES >= BN * TILE_N * 2, "the y staging tile reuses the token ring");
+    static constexpr int SMEM = XS * X_STAGE + R * RAW_STAGE + BAR_BYTES + 1024;
+    static_assert(XS * X_STAGE >= BN * TILE_N * 2, "the y staging tile reuses the token ring");
 };
 
 struct TcFwdParams {
@@ -142,16 +161,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   const TcFwdParams p)
 {
     using C = Cfg<BN>;
+    constexpr int SPS = C::SPS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *X_ring = smem;
-    uint8_t *R_ring = X_ring + C::S * C::X_BYTES;
+    uint8_t *R_ring = X_ring + C::XS * C::X_STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(R_ring + C::R * RAW_STAGE);
     uint64_t *raw_full = bars;
     uint64_t *raw_empty = raw_full + C::R;
     uint64_t *x_full = raw_empty + C::R;
-    uint64_t *a_full = x_full + C::S;
-    uint64_t *stage_empty = a_full + C::S;  // MMA of the stage done: frees its A and token tiles
+    uint64_t *x_empty = x_full + C::XS;      // MMA of the stage done: frees its token tile
+    uint64_t *a_full = x_empty + C::XS;
+    uint64_t *stage_empty = a_full + C::S;  // MMA of the stage done: frees its A tile
     uint64_t *acc_full = stage_empty + C::S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -165,9 +186,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n0 = n_tile * TILE_N, m0 = m_tile * BN;
     const int k_begin = split * p.steps_per_split;  // a multiple of GK
     const int k_end = min(p.nk, k_begin + p.steps_per_split);
-    const int n_main = k_end > k_begin ? k_end - k_begin : 0;
-    const int n_groups = (n_main + GK - 1) / GK;  // n_main is a multiple of GK (K % 256 == 0)
+    const int n_main = k_end > k_begin ? k_end - k_begin : 0;  // a multiple of GK (K % 256 == 0)
+    const int n_groups = n_main / GK;
     const int n_steps = n_main + (split == p.splits - 1 ? p.lora_steps : 0);
+    const int n_stages = (n_steps + SPS - 1) / SPS;  // the last (LoRA) stage may be partial
+    const int main_stages = n_main / SPS;
     // Every CTA walks its k-range from a different raw group, so that the CTAs
     // do not all read the same token tile from L2 at the same time.
     const int grot = n_groups > 0 ? (n_tile * 5 + m_tile * 3) % n_groups : 0;
@@ -176,10 +199,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::R; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], NUM_DQ_WARPS);
+            mbar_init(&raw_empty[i], C::RAW_CONSUMERS);
+        }
+        for (int i = 0; i < C::XS; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
         }
         for (int i = 0; i < C::S; ++i) {
-            mbar_init(&x_full[i], 1);
             mbar_init(&a_full[i], DQ_GROUP_WARPS);
             mbar_init(&stage_empty[i], 1);
         }
@@ -208,9 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Bounded wait for the phase with this parity; false once the CTA aborts.
     // Waiting threads poll with a short sleep between tries rather than
-    // spinning: the dequantizing warps are issue-bound, and a spinning waiter
-    // (a role thread, or the dequant group whose turn it is not) takes their
-    // scheduler slots.
+    // spinning: a spinning waiter takes the dequantizing warps' issue slots.
     const unsigned sleep_ns = warp >= NUM_DQ_WARPS ? 64u : 32u;
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         if (mbar_try_wait(bar, parity)) return true;
@@ -254,130 +278,154 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == WARP_X) {
-        // ------------------------------------------- token tiles
+        // ------------------------------------------- token tiles (SPS per stage)
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             int issued = 0;
-            for (int i = 0; i < n_steps; ++i) {
-                const int slot = i % C::S;
-                const uint32_t round = (uint32_t)(i / C::S);
+            for (int j = 0; j < n_stages; ++j) {
+                const int slot = j & (C::XS - 1);
+                const uint32_t round = (uint32_t)(j >> C::LOG_XS);
                 // u is written by the LoRA down-projection launched just before
                 // this kernel, which lets this grid start early (programmatic
                 // launch): wait for that grid only before the first u tile.  The
                 // token tiles x were complete before that grid was launched.
-                if (i == n_main) asm volatile("griddepcontrol.wait;" ::: "memory");
-                if (round > 0 && !wait(&stage_empty[slot], (round - 1) & 1u)) break;
-                mbar_arrive_expect_tx(&x_full[slot], C::X_BYTES);
-                uint8_t *dst = X_ring + slot * C::X_BYTES;
-                if (i < n_main)
-                    tma_load_2d_hint(dst, &x_map, &x_full[slot], kstep(i) * BK, m0, pol);
-                else
-                    tma_load_2d_hint(dst, &u_map, &x_full[slot], (i - n_main) * BK, m0, pol);
-                issued = i + 1;
+                if (j == main_stages) asm volatile("griddepcontrol.wait;" ::: "memory");
+                if (round > 0 && !wait(&x_empty[slot], (round - 1) & 1u)) break;
+                const int nsub = min(SPS, n_steps - j * SPS);
+                mbar_arrive_expect_tx(&x_full[slot], (uint32_t)(C::X_STEP * nsub));
+                uint8_t *dst = X_ring + slot * C::X_STAGE;
+#pragma unroll
+                for (int sub = 0; sub < SPS; ++sub) {
+                    if (sub >= nsub) break;
+                    const int i = j * SPS + sub;
+                    if (i < n_main)
+                        tma_load_2d_hint(dst + sub * C::X_STEP, &x_map, &x_full[slot], kstep(i) * BK, m0, pol);
+                    else
+                        tma_load_2d_hint(dst + sub * C::X_STEP, &u_map, &x_full[slot], (i - n_main) * BK, m0, pol);
+                }
+                issued = j + 1;
             }
             if (*abort_flag)
-                for (int i = issued > C::S ? issued - C::S : 0; i < issued; ++i)
-                    drain_wait(&x_full[i % C::S], (uint32_t)(i / C::S) & 1u);
+                for (int j = issued > C::XS ? issued - C::XS : 0; j < issued; ++j)
+                    drain_wait(&x_full[j & (C::XS - 1)], (uint32_t)(j >> C::LOG_XS) & 1u);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
         // ------------------------------------------- MMA issue
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(TILE_N, BN);
-            // An mbarrier query costs the issuing thread ~80 cycles of latency, as
-            // long as four small MMAs: the next step's barriers are probed before
-            // this step's MMAs are issued, and waited on only if the probe failed.
-            bool ready = n_steps > 0 && wait(&a_full[0], 0) && wait(&x_full[0], 0);
-            for (int i = 0; i < n_steps && ready; ++i) {
-                const int s = i % C::S;
-                const int s1 = (i + 1) % C::S;
-                const uint32_t par1 = (uint32_t)((i + 1) / C::S) & 1u;
-                const bool more = i + 1 < n_steps;
-                const bool pa = more && mbar_try_wait(&a_full[s1], par1);
-                const bool px = more && mbar_try_wait(&x_full[s1], par1);
-                tc_fence_after();
-                const uint32_t at = tmem + (uint32_t)(C::A_COL0 + s * 32);
-                const uint64_t bd = desc_kmajor_sw128(smem_u32(X_ring + s * C::X_BYTES));
+        // The whole warp runs the loop (stage indices and descriptors stay
+        // warp-uniform); one elected lane issues the MMAs and the commit.
+        constexpr uint32_t idesc = idesc_bf16_f32(TILE_N, BN);
+        const uint64_t bd0 = desc_kmajor_sw128(smem_u32(X_ring));
+        const uint32_t at0 = tmem + (uint32_t)C::A_COL0;
+        bool ready = n_stages > 0 && __all_sync(0xFFFFFFFFu, wait(&a_full[0], 0) && wait(&x_full[0], 0));
+        for (int j = 0; j < n_stages && ready; ++j) {
+            const int s = j & (C::S - 1), xs = j & (C::XS - 1);
+            const int nsub = min(SPS, n_steps - j * SPS);
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t at = at0 + (uint32_t)(s * 32 * SPS);
+                const uint64_t bd = bd0 + (uint64_t)((xs * C::X_STAGE) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)  // 16 k = 8 TMEM columns of A
-                    umma_bf16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                for (int sub = 0; sub < SPS; ++sub) {
+                    if (sub >= nsub) break;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // 16 k = 8 TMEM columns of A, 32 bytes of B
+                        umma_bf16_ts(tmem, at + (uint32_t)(sub * 32 + 8 * kk),
+                                     bd + (uint64_t)((sub * C::X_STEP) >> 4) + 2u * kk, idesc,
+                                     (j > 0 || sub > 0 || kk > 0) ? 1u : 0u);
+                }
                 umma_commit(&stage_empty[s]);
-                if (more) ready = (pa || wait(&a_full[s1], par1)) && (px || wait(&x_full[s1], par1));
+                umma_commit(&x_empty[xs]);
             }
-            // Arrives once every MMA issued above has completed (also after an abort).
-            umma_commit(acc_full);
+            __syncwarp();
+            if (j + 1 < n_stages) {
+                const int s1 = (j + 1) & (C::S - 1), xs1 = (j + 1) & (C::XS - 1);
+                ready = __all_sync(0xFFFFFFFFu, wait(&a_full[s1], (uint32_t)((j + 1) >> C::LOG_S) & 1u) &&
+                                                    wait(&x_full[xs1], (uint32_t)((j + 1) >> C::LOG_XS) & 1u));
+            }
         }
+        // Arrives once every MMA issued above has completed (also after an abort).
+        if (elect_one()) umma_commit(acc_full);
         __syncwarp();
     } else {
         // ------------------------------------------- dequantize
-        // Group g = warp / 4 takes the steps i = g, g + DQ_GROUPS, ...; thread =
-        // one weight row of the tile, all 64 k of the step (32 code bytes).
+        // Group g = warp / 4 takes the stages j = g, g + DQ_GROUPS, ...; thread =
+        // one weight row of the tile, all 64 k of each of the stage's SPS steps.
         const int row = (warp & 3) * 32 + lane;
         const int group = warp >> 2;
         const int n = n0 + row;
         const bool row_ok = n < p.N;
         const float pow2 = pow2f(126 - tc_exponent_offset(*p.tensor_scale));
-        for (int i = group; i < n_steps; i += DQ_GROUPS) {
-            uint32_t out[32];
-            if (i < n_main) {
-                const int g = i / GK, rs = g % C::R, q = i % GK;
-                const bool first_in_stage = q < DQ_GROUPS;  // this group's first step of the raw stage
-                if (first_in_stage && !__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(g / C::R) & 1u))) break;
-                // codes: row `row`, logical 16-byte chunks 2q and 2q+1 of the 128-byte
-                // row, stored by TMA at chunk ^ (row % 8)
-                const uint32_t rb = smem_u32(R_ring + rs * RAW_STAGE) + row * 128;
-                const uint4 c0 = ld_shared_v4(rb + (uint32_t)(((2 * q) ^ (row & 7)) * 16));
-                const uint4 c1 = ld_shared_v4(rb + (uint32_t)(((2 * q + 1) ^ (row & 7)) * 16));
-                const uint32_t sc =
-                    *reinterpret_cast<const uint32_t *>(R_ring + rs * RAW_STAGE + RAW_CODES + row * 16 + q * 4);
-                if (q >= GK - DQ_GROUPS || i + DQ_GROUPS >= n_main) {  // this group's last step of the raw stage
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&raw_empty[rs]);
-                }
-                const uint32_t f0 = scale_factor_bf16x2(sc & 0xFFu, pow2);
-                const uint32_t f1 = scale_factor_bf16x2((sc >> 8) & 0xFFu, pow2);
-                const uint32_t f2 = scale_factor_bf16x2((sc >> 16) & 0xFFu, pow2);
-                const uint32_t f3 = scale_factor_bf16x2(sc >> 24, pow2);
-                dequant_word(c0.x, f0, out + 0);
-                dequant_word(c0.y, f0, out + 4);
-                dequant_word(c0.z, f1, out + 8);
-                dequant_word(c0.w, f1, out + 12);
-                dequant_word(c1.x, f2, out + 16);
-                dequant_word(c1.y, f2, out + 20);
-                dequant_word(c1.z, f3, out + 24);
-                dequant_word(c1.w, f3, out + 28);
-            } else {
-                // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
-                const int j0 = (i - n_main) * BK;
-                const __nv_bfloat16 *b = p.Bl + (size_t)(row_ok ? n : 0) * p.r + j0;
-                if (row_ok && (p.r & 7) == 0 && j0 + 64 <= p.r) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(b) + q);
-                        out[4 * q] = v.x;
-                        out[4 * q + 1] = v.y;
-                        out[4 * q + 2] = v.z;
-                        out[4 * q + 3] = v.w;
-                    }
-                } else {
-                    const uint16_t *bh = reinterpret_cast<const uint16_t *>(b);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const uint32_t lo = (row_ok && j0 + 2 * q < p.r) ? bh[2 * q] : 0u;
-                        const uint32_t hi = (row_ok && j0 + 2 * q + 1 < p.r) ? bh[2 * q + 1] : 0u;
-                        out[q] = lo | (hi << 16);
-                    }
-                }
-            }
-            const int s = i % C::S;
-            const uint32_t sround = (uint32_t)(i / C::S);
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        for (int j = group; j < n_stages; j += DQ_GROUPS) {
+            const int s = j % C::S;
+            const uint32_t sround = (uint32_t)(j / C::S);
+            const bool main_stage = j < main_stages;
+            const int g = (j * SPS) / GK, rs = g % C::R;  // raw stage of a main stage
+            // Stage free first: the MMA is then past stage j - S, so every raw stage
+            // up to g - R has landed and the raw_full parity below cannot alias.
             if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&stage_empty[s], (sround - 1) & 1u))) break;
-            // row `row` of the A stage: TMEM lane `row`, 32 columns of bf16 pairs
-            tmem_st32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(C::A_COL0 + s * 32), out);
+            if (main_stage && !__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(g / C::R) & 1u))) break;
+            const int nsub = min(SPS, n_steps - j * SPS);
+#pragma unroll
+            for (int sub = 0; sub < SPS; ++sub) {
+                if (sub >= nsub) break;
+                const int i = j * SPS + sub;
+                uint32_t out[32];
+                if (main_stage) {
+                    const int q = i % GK;
+                    // codes: row `row`, logical 16-byte chunks 2q and 2q+1 of the 128-byte
+                    // row, stored by TMA at chunk ^ (row % 8)
+                    const uint32_t rb = smem_u32(R_ring + rs * RAW_STAGE) + row * 128;
+                    const uint4 c0 = ld_shared_v4(rb + (uint32_t)(((2 * q) ^ (row & 7)) * 16));
+                    const uint4 c1 = ld_shared_v4(rb + (uint32_t)(((2 * q + 1) ^ (row & 7)) * 16));
+                    const uint32_t sc = ld_shared_u32(smem_u32(R_ring + rs * RAW_STAGE + RAW_CODES) + row * 16 + q * 4);
+                    const uint32_t f0 = scale_factor_bf16x2(sc & 0xFFu, pow2);
+                    const uint32_t f1 = scale_factor_bf16x2((sc >> 8) & 0xFFu, pow2);
+                    const uint32_t f2 = scale_factor_bf16x2((sc >> 16) & 0xFFu, pow2);
+                    const uint32_t f3 = scale_factor_bf16x2(sc >> 24, pow2);
+                    dequant_word(c0.x, f0, out + 0);
+                    dequant_word(c0.y, f0, out + 4);
+                    dequant_word(c0.z, f1, out + 8);
+                    dequant_word(c0.w, f1, out + 12);
+                    dequant_word(c1.x, f2, out + 16);
+                    dequant_word(c1.y, f2, out + 20);
+                    dequant_word(c1.z, f3, out + 24);
+                    dequant_word(c1.w, f3, out + 28);
+                } else {
+                    // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
+                    const int j0 = (i - n_main) * BK;
+                    const __nv_bfloat16 *b = p.Bl + (size_t)(row_ok ? n : 0) * p.r + j0;
+                    if (row_ok && (p.r & 7) == 0 && j0 + 64 <= p.r) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(b) + q);
+                            out[4 * q] = v.x;
+                            out[4 * q + 1] = v.y;
+                            out[4 * q + 2] = v.z;
+                            out[4 * q + 3] = v.w;
+                        }
+                    } else {
+                        const uint16_t *bh = reinterpret_cast<const uint16_t *>(b);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const uint32_t lo = (row_ok && j0 + 2 * q < p.r) ? bh[2 * q] : 0u;
+                            const uint32_t hi = (row_ok && j0 + 2 * q + 1 < p.r) ? bh[2 * q + 1] : 0u;
+                            out[q] = lo | (hi << 16);
+                        }
+                    }
+                }
+                // row `row` of the step's A tile: TMEM lane `row`, 32 columns of bf16 pairs
+                tmem_st32(trow + (uint32_t)(C::A_COL0 + s * 32 * SPS + sub * 32), out);
+            }
+            if (main_stage) {  // every group's stage is its only one in the raw stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            const bool withhold = p.fault && blockIdx.x == 0 && warp == 0 && i == 0;
+            const bool withhold = p.fault && blockIdx.x == 0 && warp == 0 && j == 0;
             if (lane == 0 && !withhold) mbar_arrive(&a_full[s]);
         }
 
