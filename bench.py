@@ -235,11 +235,15 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.profile_region:  # lets `ncu --profile-from-start off` see only the timed steps
+        torch.cuda.cudart().cudaProfilerStart()
     t0.record()
     for i in range(args.steps):
         graphs[i % n_copies].replay()
     t1.record()
     torch.cuda.synchronize()
+    if args.profile_region:
+        torch.cuda.cudart().cudaProfilerStop()
     barrier()
     clk = clocks.stop()
     assert q.get_error() == 0
@@ -386,6 +390,8 @@ def main():
     ap.add_argument("--M", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-region", action="store_true",
+                    help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_init()

@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool ok_warp = __all_sync(0xFFFFFFFFu, wait(acc_full, 0));
             if (lane == 0) ep_ok[warp] = ok_warp ? 1 : 0;
             named_bar_sync(1, 128);  // one decision for all four epilogue warps
-            const bool ok = ep_ok[0] && ep_ok[1] && ep_ok[2] && ep_ok[3];
+            const bool ok = ep_ok[0] && ep_ok[1] && ep_ok[2] && ep_ok[3] && !*abort_flag;
             tc_fence_after();
             asm volatile("griddepcontrol.wait;" ::: "memory");  // the workspace and y follow the predecessor
             if (ok) {
