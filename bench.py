@@ -31,6 +31,24 @@ import torch  # noqa: E402
 L2_BYTES = 129 * 1024 * 1024
 
 
+# DRAM bytes (read + write) per launch of the forward kernel, from one ncu capture
+# (profiles/tc_fwd_decode_qwen7b_m64.md) of csrc/linear_tc.cu with this sha256
+# prefix; reported as roofline.traffic only while the source still matches.
+NCU_KERNEL_SHA = "b236bc07ce620985"
+NCU_DRAM_BYTES = {"gate_proj": 39.944704e6, "up_proj": 39.947264e6, "down_proj": 40.938240e6}
+
+
+def ncu_traffic(name):
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "nvfp4_weight_only_quantize_gb300", "csrc",
+                       "linear_tc.cu")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return NCU_DRAM_BYTES.get(name) if sha == NCU_KERNEL_SHA else None
+
+
 def linear_bytes(N, K, r):
     return N * K * 0.5625 + 4 + 2 * r * (N + K)
 
@@ -306,7 +324,8 @@ def run_ours(args, rank, world, local_rank):
         "per_linear": per_linear,
         "roofline": {"bound": "hbm", "kernel": f"linear fwd {dom} {dN}x{dK} (M={M}, r={wl.r})",
                      "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)", "traffic": None},
+                     "peak_source": f"{peak_kind} hbm_gbs (burst copy)", "traffic": ncu_traffic(dom),
+                     "algorithmic_bytes": linear_bytes(dN, dK, wl.r)},
         "e2e": {"value": round(e2e_units / e2e_secs / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * M * wl.hidden * 2, "d2h_bytes_per_step": M * wl.hidden * 2},
         "gpu_launches": kernels_per_step * args.steps,
