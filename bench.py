@@ -138,10 +138,11 @@ class ClockSampler:
 class DecodeLayer:
     """NVFP4 weights + LoRA adapters + norm scales of n_copies Qwen2.5-7B layers."""
 
-    def __init__(self, wl, n_copies, device):
+    def __init__(self, wl, n_copies, device, packed=True):
         import nvfp4_weight_only_quantize_gb300 as q
         from nvfp4_weight_only_quantize_gb300 import synth
         self.q, self.wl, self.copies = q, wl, []
+        self.fwd = q.qerl_nvfp4_lora_linear_fwd_packed if packed else q.qerl_nvfp4_lora_linear_fwd
         for c in range(n_copies):
             lins = []
             for i, (name, N, K) in enumerate(wl.linears):
@@ -149,6 +150,8 @@ class DecodeLayer:
                 W = synth.weight(N, K, base + synth.T_W, device)
                 codes, scales, ts = q.qerl_nvfp4_quantize(W)
                 del W
+                if packed:  # once, when the frozen weight is loaded
+                    q.qerl_nvfp4_pack_codes(codes, out=codes)
                 A = synth.lora_A(wl.r, K, base + synth.T_A, device)
                 B = synth.lora_B(N, wl.r, base + synth.T_B, device)
                 lins.append((name, N, K, codes, scales, ts, A, B))
@@ -183,8 +186,7 @@ class DecodeLayer:
             if ev is not None:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
-            q.qerl_nvfp4_lora_linear_fwd(src[name], codes, scales, ts, A, B, self.wl.lora_scale, y=o[name],
-                                         ws=buf["ws"])
+            self.fwd(src[name], codes, scales, ts, A, B, self.wl.lora_scale, y=o[name], ws=buf["ws"])
             if ev is not None:
                 e1.record()
                 ev.setdefault(name, []).append((e0, e1))
@@ -225,7 +227,7 @@ def run_ours(args, rank, world, local_rank):
     M = args.M
     per_copy = sum(N * K * 0.5625 for _, N, K in wl.linears)
     n_copies = max(2, int(3 * L2_BYTES // per_copy) + 1)
-    layer = DecodeLayer(wl, n_copies, dev)
+    layer = DecodeLayer(wl, n_copies, dev, packed=args.codes == "packed")
     buf = layer.buffers(M, dev)
     x = synth.activations(M, wl.hidden, synth.seed_of(1, 0, synth.T_X), dev)
     attn = synth.activations(M, wl.hidden, synth.seed_of(1, 1, synth.T_X), dev)
@@ -278,7 +280,7 @@ def run_ours(args, rank, world, local_rank):
         def run_lin(li=li, xin=xin, yout=yout):
             for c in range(n_copies):
                 _, _, _, codes, scales, ts, A, B = layer.copies[c][0][li]
-                q.qerl_nvfp4_lora_linear_fwd(xin, codes, scales, ts, A, B, wl.lora_scale, y=yout, ws=buf["ws"])
+                layer.fwd(xin, codes, scales, ts, A, B, wl.lora_scale, y=yout, ws=buf["ws"])
         g = _graph(run_lin)
         _time_graph(g, 3)
         reps = 20
@@ -318,6 +320,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies, "
                          f"{n_copies * per_copy / 2**20:.0f} MiB NVFP4 > 129 MiB L2",
                    "launch": "one CUDA graph per step (per weight copy)",
+                   "codes": args.codes + " layout (packed once when the weights are loaded)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(M * args.steps * world / max_secs, 1),
         "pct_of_hbm_peak": round(100 * value / world / hbm, 2),
@@ -409,6 +412,8 @@ def main():
     ap.add_argument("--M", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--codes", default="packed", choices=["packed", "standard"],
+                    help="code layout of the frozen weights (packed once at load time, or as quantized)")
     ap.add_argument("--profile-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     args = ap.parse_args()

@@ -183,6 +183,44 @@ qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x, int64_t M,
                                        size_t ws_bytes, qerl_stream_t stream);
 
 /*
+ * Packed code layout for the tensor-core dequantizer.  The pages name Marlin as
+ * the kernel that serves the NVFP4 x BF16 product ("QeRL" README mirror,
+ * feature list; dataforcee, RL-loop section); kernels of that family lay the
+ * frozen weight out once, when it is loaded, in the order their dequantizer
+ * reads it.  This is that step for this library: a bit permutation inside each
+ * little-endian 32-bit word of codes (eight codes of k = 8w .. 8w+7), so the
+ * packed array has the same size and shape as the standard one [N, K/2]:
+ *   elements 2p, 2p+1 form pair p = 0..3; the even element's mantissa, low
+ *   exponent and high exponent bits sit at bits (6,7,8), (3,4,5), (0,1,2),
+ *   (9,10,11) for p = 0,1,2,3 and its sign at bit 15, 12, 13, 14; the odd
+ *   element uses the same positions + 16.
+ * Scales and the tensor scale are unchanged.
+ *   codes/packed (device) [N, K/2] bytes, 16-byte aligned; K % 16 == 0
+ *   (QERL_ERR_SHAPE).  in == out (in place) is allowed; other overlaps return
+ *   QERL_ERR_INVALID_ARG.
+ */
+qerl_status qerl_nvfp4_pack_codes(const uint8_t *codes, int64_t N, int64_t K, uint8_t *packed,
+                                  qerl_stream_t stream);
+qerl_status qerl_nvfp4_unpack_codes(const uint8_t *packed, int64_t N, int64_t K, uint8_t *codes,
+                                    qerl_stream_t stream);
+
+/*
+ * qerl_nvfp4_lora_linear_fwd and qerl_nvfp4_lora_linear_bwd with the codes in
+ * the packed layout above: same arguments, same results, same workspace sizes.
+ */
+qerl_status qerl_nvfp4_lora_linear_fwd_packed(const void *x, int64_t M, int64_t K, int64_t N,
+                                              const uint8_t *packed_codes, const uint8_t *scales,
+                                              const float *tensor_scale, const void *A, const void *B,
+                                              int r, float lora_scale, void *y, float *t_out,
+                                              void *ws, size_t ws_bytes, qerl_stream_t stream);
+qerl_status qerl_nvfp4_lora_linear_bwd_packed(const void *dy, const void *x, int64_t M, int64_t K,
+                                              int64_t N, const uint8_t *packed_codes, const uint8_t *scales,
+                                              const float *tensor_scale, const void *A, const void *B,
+                                              int r, float lora_scale, const float *t_saved, void *dx,
+                                              float *dA, float *dB, int accumulate_grads, void *ws,
+                                              size_t ws_bytes, qerl_stream_t stream);
+
+/*
  * AQN-RMSNorm (1kpapers summary; dataforcee AQN paragraph: channel-wise
  * Gaussian noise in the norm's scale parameters):
  *     y[m, c] = x[m, c] / sqrt(mean_c x[m, :]^2 + eps) * (gamma[c] + sigma * z[c])

@@ -29,7 +29,8 @@ ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
 
 # Every C symbol include/qerl.h declares (checked by the CPU test suite).
 EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_linear_fwd",
-            "qerl_nvfp4_lora_linear_fwd_noalloc",
+            "qerl_nvfp4_lora_linear_fwd_noalloc", "qerl_nvfp4_pack_codes", "qerl_nvfp4_unpack_codes",
+            "qerl_nvfp4_lora_linear_fwd_packed", "qerl_nvfp4_lora_linear_bwd_packed",
             "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_noise", "qerl_aqn_sigma",
             "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
             "qerl_launch_count"]
@@ -74,6 +75,8 @@ def lib() -> C.CDLL:
                                                         vp], i32),
                 "qerl_nvfp4_lora_linear_bwd": ([vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp,
                                                 vp, vp, i32, vp, sz, vp], i32),
+                "qerl_nvfp4_pack_codes": ([vp, i64, i64, vp, vp], i32),
+                "qerl_nvfp4_unpack_codes": ([vp, i64, i64, vp, vp], i32),
                 "qerl_aqn_rmsnorm": ([vp, i64, i64, vp, f32, f32, u64, u64, u32, vp, vp, sz, vp], i32),
                 "qerl_aqn_noise": ([i64, u64, u64, u32, vp, vp, vp], i32),
                 "qerl_aqn_sigma": ([i64, i64, f32, f32, i32], f32),
@@ -83,6 +86,8 @@ def lib() -> C.CDLL:
                 "qerl_set_linear_algo": ([i32], i32),
                 "qerl_launch_count": ([], u64),
             }
+            sig["qerl_nvfp4_lora_linear_fwd_packed"] = sig["qerl_nvfp4_lora_linear_fwd"]
+            sig["qerl_nvfp4_lora_linear_bwd_packed"] = sig["qerl_nvfp4_lora_linear_bwd"]
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -156,17 +161,44 @@ def qerl_nvfp4_dequantize(codes, scales, tensor_scale, N: int, K: int, apply_ten
 
 
 # ---------------------------------------------------------------- linear
-def qerl_nvfp4_lora_linear_fwd(x, codes, scales, tensor_scale, A, B, lora_scale: float, y=None, t_out=None,
-                               ws=None, stream=None):
-    """y = x w_hat^T + s (x A^T) B^T.  x bf16 [M,K], A bf16 [r,K], B bf16 [N,r] -> y bf16 [M,N]."""
+def _fwd(name, x, codes, scales, tensor_scale, A, B, lora_scale, y, t_out, ws, stream):
     M, K = x.shape
     N, r = B.shape
     y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
     ws = workspace(OP_LINEAR_FWD, M, N, K, r, x.device) if ws is None else ws
-    _check(lib().qerl_nvfp4_lora_linear_fwd(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A), _p(B),
-                                            r, float(lora_scale), _p(y), _p(t_out), _p(ws), ws.numel(),
-                                            _stream(stream)), "qerl_nvfp4_lora_linear_fwd")
+    _check(getattr(lib(), name)(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A), _p(B), r,
+                                float(lora_scale), _p(y), _p(t_out), _p(ws), ws.numel(), _stream(stream)), name)
     return y
+
+
+def qerl_nvfp4_lora_linear_fwd(x, codes, scales, tensor_scale, A, B, lora_scale: float, y=None, t_out=None,
+                               ws=None, stream=None):
+    """y = x w_hat^T + s (x A^T) B^T.  x bf16 [M,K], A bf16 [r,K], B bf16 [N,r] -> y bf16 [M,N]."""
+    return _fwd("qerl_nvfp4_lora_linear_fwd", x, codes, scales, tensor_scale, A, B, lora_scale, y, t_out, ws, stream)
+
+
+def qerl_nvfp4_lora_linear_fwd_packed(x, packed_codes, scales, tensor_scale, A, B, lora_scale: float, y=None,
+                                      t_out=None, ws=None, stream=None):
+    """The forward with the codes in the packed layout (qerl_nvfp4_pack_codes)."""
+    return _fwd("qerl_nvfp4_lora_linear_fwd_packed", x, packed_codes, scales, tensor_scale, A, B, lora_scale, y,
+                t_out, ws, stream)
+
+
+def qerl_nvfp4_pack_codes(codes, out=None, stream=None):
+    """Standard NVFP4 codes [N, K/2] -> the packed layout (same shape; out may be codes itself)."""
+    N, half = codes.shape
+    out = torch.empty_like(codes) if out is None else out
+    _check(lib().qerl_nvfp4_pack_codes(_p(codes), N, 2 * half, _p(out), _stream(stream)), "qerl_nvfp4_pack_codes")
+    return out
+
+
+def qerl_nvfp4_unpack_codes(packed, out=None, stream=None):
+    """Inverse of qerl_nvfp4_pack_codes."""
+    N, half = packed.shape
+    out = torch.empty_like(packed) if out is None else out
+    _check(lib().qerl_nvfp4_unpack_codes(_p(packed), N, 2 * half, _p(out), _stream(stream)),
+           "qerl_nvfp4_unpack_codes")
+    return out
 
 
 def qerl_nvfp4_lora_linear_fwd_noalloc(x, codes, scales, tensor_scale, A, B, lora_scale: float, y=None,
@@ -186,6 +218,20 @@ def qerl_nvfp4_lora_linear_bwd(dy, x, codes, scales, tensor_scale, A, B, lora_sc
                                dx=None, dA=None, dB=None, accumulate: bool = False, want=("dx", "dA", "dB"),
                                ws=None, stream=None):
     """Returns (dx bf16 [M,K], dA f32 [r,K], dB f32 [N,r]); outputs not in ``want`` are None."""
+    return _bwd("qerl_nvfp4_lora_linear_bwd", dy, x, codes, scales, tensor_scale, A, B, lora_scale, t_saved, dx, dA,
+                dB, accumulate, want, ws, stream)
+
+
+def qerl_nvfp4_lora_linear_bwd_packed(dy, x, packed_codes, scales, tensor_scale, A, B, lora_scale: float,
+                                      t_saved=None, dx=None, dA=None, dB=None, accumulate: bool = False,
+                                      want=("dx", "dA", "dB"), ws=None, stream=None):
+    """The backward with the codes in the packed layout."""
+    return _bwd("qerl_nvfp4_lora_linear_bwd_packed", dy, x, packed_codes, scales, tensor_scale, A, B, lora_scale,
+                t_saved, dx, dA, dB, accumulate, want, ws, stream)
+
+
+def _bwd(name, dy, x, codes, scales, tensor_scale, A, B, lora_scale, t_saved, dx, dA, dB, accumulate, want, ws,
+         stream):
     M, N = dy.shape
     K = x.shape[1]
     r = A.shape[0]
@@ -197,10 +243,9 @@ def qerl_nvfp4_lora_linear_bwd(dy, x, codes, scales, tensor_scale, A, B, lora_sc
     if dB is None and "dB" in want:
         dB = torch.zeros(N, r, dtype=torch.float32, device=dev)
     ws = workspace(OP_LINEAR_BWD, M, N, K, r, dev) if ws is None else ws
-    _check(lib().qerl_nvfp4_lora_linear_bwd(_p(dy), _p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A),
-                                            _p(B), r, float(lora_scale), _p(t_saved), _p(dx), _p(dA), _p(dB),
-                                            int(accumulate), _p(ws), ws.numel(), _stream(stream)),
-           "qerl_nvfp4_lora_linear_bwd")
+    _check(getattr(lib(), name)(_p(dy), _p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A), _p(B), r,
+                                float(lora_scale), _p(t_saved), _p(dx), _p(dA), _p(dB), int(accumulate), _p(ws),
+                                ws.numel(), _stream(stream)), name)
     return dx, dA, dB
 
 

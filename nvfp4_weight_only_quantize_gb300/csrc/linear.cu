@@ -11,6 +11,7 @@
 #include <atomic>
 
 #include "linear.cuh"
+#include "packed_layout.cuh"
 
 namespace qerl {
 namespace {
@@ -34,21 +35,30 @@ struct ColF32 {  // (p, k) -> base[k * ld + p]
     __device__ float operator()(int64_t p, int64_t k) const { return base[k * ld + p]; }
 };
 // w'(n, k) = e2m1(code) * e4m3(block scale), the weight without its tensor scale.
-__device__ __forceinline__ float wprime(const uint8_t *codes, const uint8_t *scales, int64_t K, int64_t n, int64_t k)
+__device__ __forceinline__ float wprime(const uint8_t *codes, const uint8_t *scales, int64_t K, int64_t n, int64_t k,
+                                        int packed)
 {
-    const uint32_t byte = codes[n * (K / 2) + k / 2];
-    const uint32_t c = (k & 1) ? (byte >> 4) : (byte & 15u);
+    uint32_t c;
+    if (packed) {
+        const uint32_t w = reinterpret_cast<const uint32_t *>(codes)[n * (K / 8) + k / 8];
+        c = packed_code(w, (int)(k & 7));
+    } else {
+        const uint32_t byte = codes[n * (K / 2) + k / 2];
+        c = (k & 1) ? (byte >> 4) : (byte & 15u);
+    }
     return e2m1_to_float(c) * e4m3_to_float(scales[n * (K / 16) + k / 16]);
 }
 struct WRow {  // (n, k)
     const uint8_t *codes, *scales;
     int64_t K;
-    __device__ float operator()(int64_t n, int64_t k) const { return wprime(codes, scales, K, n, k); }
+    int packed;
+    __device__ float operator()(int64_t n, int64_t k) const { return wprime(codes, scales, K, n, k, packed); }
 };
 struct WCol {  // (k, n)
     const uint8_t *codes, *scales;
     int64_t K;
-    __device__ float operator()(int64_t k, int64_t n) const { return wprime(codes, scales, K, n, k); }
+    int packed;
+    __device__ float operator()(int64_t k, int64_t n) const { return wprime(codes, scales, K, n, k, packed); }
 };
 
 // ------------------------------------------------------------ epilogues
@@ -155,7 +165,7 @@ qerl_status simt_fwd(const FwdArgs &a, char *ws, cudaStream_t s)
 {
     float *t = a.t_out ? a.t_out : reinterpret_cast<float *>(ws);
     QERL_TRY(run_gemm(a.M, a.r, a.K, RowBF16{a.x, a.K}, RowBF16{a.A, a.K}, StoreF32{t, a.r, 1.0f, 0}, s));
-    return run_gemm(a.M, a.N, a.K, RowBF16{a.x, a.K}, WRow{a.codes, a.scales, a.K},
+    return run_gemm(a.M, a.N, a.K, RowBF16{a.x, a.K}, WRow{a.codes, a.scales, a.K, a.packed},
                     FwdEpi{a.y, a.N, a.tensor_scale, t, a.B, a.r, a.lora_scale}, s);
 }
 
@@ -165,7 +175,7 @@ qerl_status simt_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     float *u = reinterpret_cast<float *>(ws + round256(size_t(a.M) * a.r * sizeof(float)));
     QERL_TRY(run_gemm(a.M, a.r, a.N, RowBF16{a.dy, a.N}, ColBF16{a.B, a.r}, StoreF32{v, a.r, 1.0f, 0}, s));
     if (a.dx)
-        QERL_TRY(run_gemm(a.M, a.K, a.N, RowBF16{a.dy, a.N}, WCol{a.codes, a.scales, a.K},
+        QERL_TRY(run_gemm(a.M, a.K, a.N, RowBF16{a.dy, a.N}, WCol{a.codes, a.scales, a.K, a.packed},
                           DxEpi{a.dx, a.K, a.tensor_scale, v, a.A, a.r, a.lora_scale}, s));
     if (a.dA)
         QERL_TRY(run_gemm((int64_t)a.r, a.K, a.M, ColF32{v, a.r}, ColBF16{a.x, a.K},
@@ -243,11 +253,11 @@ extern "C" qerl_status qerl_set_linear_algo(int algo)
     return QERL_OK;
 }
 
-extern "C" qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
-                                                  const uint8_t *codes, const uint8_t *scales,
-                                                  const float *tensor_scale, const void *A, const void *B, int r,
-                                                  float lora_scale, void *y, float *t_out, void *ws, size_t ws_bytes,
-                                                  qerl_stream_t stream)
+namespace {
+
+qerl_status fwd_entry(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes, const uint8_t *scales,
+                      const float *tensor_scale, const void *A, const void *B, int r, float lora_scale, void *y,
+                      float *t_out, void *ws, size_t ws_bytes, qerl_stream_t stream, int packed)
 {
     QERL_TRY(check_common(M, K, N, codes, scales, tensor_scale, A, B, r));
     if (M == 0) return QERL_OK;  // x, y may be NULL for an empty batch
@@ -257,7 +267,7 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int6
     QERL_TRY(check_device());
     const FwdArgs a{static_cast<const __nv_bfloat16 *>(x), M, K, N, codes, scales, tensor_scale,
                     static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), r,
-                    lora_scale, static_cast<__nv_bfloat16 *>(y), t_out};
+                    lora_scale, static_cast<__nv_bfloat16 *>(y), t_out, packed};
     cudaStream_t s = as_cuda(stream);
     if (g_algo.load() != QERL_ALGO_SIMT) {
         const qerl_status st = tc_linear_fwd(a, static_cast<char *>(ws), ws_bytes, s);
@@ -266,12 +276,10 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int6
     return simt_fwd(a, static_cast<char *>(ws), s);
 }
 
-extern "C" qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x, int64_t M, int64_t K, int64_t N,
-                                                  const uint8_t *codes, const uint8_t *scales,
-                                                  const float *tensor_scale, const void *A, const void *B, int r,
-                                                  float lora_scale, const float *t_saved, void *dx, float *dA,
-                                                  float *dB, int accumulate_grads, void *ws, size_t ws_bytes,
-                                                  qerl_stream_t stream)
+qerl_status bwd_entry(const void *dy, const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
+                      const uint8_t *scales, const float *tensor_scale, const void *A, const void *B, int r,
+                      float lora_scale, const float *t_saved, void *dx, float *dA, float *dB, int accumulate_grads,
+                      void *ws, size_t ws_bytes, qerl_stream_t stream, int packed)
 {
     QERL_TRY(check_common(M, K, N, codes, scales, tensor_scale, A, B, r));
     if (M > 0 && (!dy || !x)) return QERL_ERR_INVALID_ARG;
@@ -291,11 +299,55 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x,
     const BwdArgs a{static_cast<const __nv_bfloat16 *>(dy), static_cast<const __nv_bfloat16 *>(x), M, K, N, codes,
                     scales, tensor_scale, static_cast<const __nv_bfloat16 *>(A),
                     static_cast<const __nv_bfloat16 *>(B), r, lora_scale, t_saved,
-                    static_cast<__nv_bfloat16 *>(dx), dA, dB, accumulate_grads};
+                    static_cast<__nv_bfloat16 *>(dx), dA, dB, accumulate_grads, packed};
     cudaStream_t s = as_cuda(stream);
     if (g_algo.load() != QERL_ALGO_SIMT) {
         const qerl_status st = tc_linear_bwd(a, static_cast<char *>(ws), ws_bytes, s);
         if (st != QERL_ERR_SHAPE) return st;
     }
     return simt_bwd(a, static_cast<char *>(ws), s);
+}
+
+}  // namespace
+
+extern "C" qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
+                                                  const uint8_t *codes, const uint8_t *scales,
+                                                  const float *tensor_scale, const void *A, const void *B, int r,
+                                                  float lora_scale, void *y, float *t_out, void *ws, size_t ws_bytes,
+                                                  qerl_stream_t stream)
+{
+    return fwd_entry(x, M, K, N, codes, scales, tensor_scale, A, B, r, lora_scale, y, t_out, ws, ws_bytes, stream, 0);
+}
+
+extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_packed(const void *x, int64_t M, int64_t K, int64_t N,
+                                                         const uint8_t *packed_codes, const uint8_t *scales,
+                                                         const float *tensor_scale, const void *A, const void *B,
+                                                         int r, float lora_scale, void *y, float *t_out, void *ws,
+                                                         size_t ws_bytes, qerl_stream_t stream)
+{
+    return fwd_entry(x, M, K, N, packed_codes, scales, tensor_scale, A, B, r, lora_scale, y, t_out, ws, ws_bytes,
+                     stream, 1);
+}
+
+extern "C" qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x, int64_t M, int64_t K, int64_t N,
+                                                  const uint8_t *codes, const uint8_t *scales,
+                                                  const float *tensor_scale, const void *A, const void *B, int r,
+                                                  float lora_scale, const float *t_saved, void *dx, float *dA,
+                                                  float *dB, int accumulate_grads, void *ws, size_t ws_bytes,
+                                                  qerl_stream_t stream)
+{
+    return bwd_entry(dy, x, M, K, N, codes, scales, tensor_scale, A, B, r, lora_scale, t_saved, dx, dA, dB,
+                     accumulate_grads, ws, ws_bytes, stream, 0);
+}
+
+extern "C" qerl_status qerl_nvfp4_lora_linear_bwd_packed(const void *dy, const void *x, int64_t M, int64_t K,
+                                                         int64_t N, const uint8_t *packed_codes,
+                                                         const uint8_t *scales, const float *tensor_scale,
+                                                         const void *A, const void *B, int r, float lora_scale,
+                                                         const float *t_saved, void *dx, float *dA, float *dB,
+                                                         int accumulate_grads, void *ws, size_t ws_bytes,
+                                                         qerl_stream_t stream)
+{
+    return bwd_entry(dy, x, M, K, N, packed_codes, scales, tensor_scale, A, B, r, lora_scale, t_saved, dx, dA, dB,
+                     accumulate_grads, ws, ws_bytes, stream, 1);
 }

@@ -16,6 +16,7 @@ struct FwdArgs {
     float lora_scale;
     __nv_bfloat16 *y;
     float *t_out;
+    int packed = 0;  // codes in the packed layout (packed_layout.cuh)
 };
 
 struct BwdArgs {
@@ -30,6 +31,7 @@ struct BwdArgs {
     __nv_bfloat16 *dx;
     float *dA, *dB;
     int accumulate;
+    int packed = 0;
 };
 
 size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);

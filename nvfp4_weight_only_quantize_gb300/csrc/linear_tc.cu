@@ -120,11 +120,16 @@ __device__ __forceinline__ int tc_exponent_offset(float s_t)
 // 2^e as a float for e in the normal range (exact, unlike exp2f).
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// bf16x2 {f, f} with f = e4m3(b) * 2^(126 - c): exact (<= 4 significant bits).
-__device__ __forceinline__ uint32_t scale_factor_bf16x2(uint32_t b, float pow2)
+// bf16x2 {f, f} with f = e4m3(b) * 2^(126 - c), exact (<= 4 significant bits).
+// b20 holds the scale byte b in bits 20..27 (other bits are masked off here).
+// As FP32 bits that is e4m3(b) * 2^-120 for every byte < 0x80, subnormal
+// bytes included (they land on FP32 subnormals, which the multiply keeps), so
+// two exact multiplies by powers of two give f.
+__device__ __forceinline__ uint32_t scale_factor_bf16x2(uint32_t b20, float pow2)
 {
-    const uint32_t h = __float_as_uint(e4m3_to_float(b) * pow2) >> 16;
-    return h | (h << 16);
+    const float f = __uint_as_float(b20 & 0x0FF00000u) * pow2f(120) * pow2;
+    const uint32_t u = __float_as_uint(f);
+    return prmt(u, u, 0x3232u);  // {high half, high half}
 }
 
 // Eight E2M1 codes (one word, element 2j in the low nibble of byte j) -> four
@@ -132,8 +137,19 @@ __device__ __forceinline__ uint32_t scale_factor_bf16x2(uint32_t b, float pow2)
 // exponent/mantissa bits to bits 8..6, which as a bf16 is e2m1 * 2^-126 (the
 // code 0.5 becomes the subnormal 2^-127); one bf16x2 multiply by the block's
 // scale factor then gives e2m1 * e4m3 * 2^-c exactly.
+template <bool PACKED>
 __device__ __forceinline__ void dequant_word(uint32_t q, uint32_t f2, uint32_t *out)
 {
+    if (PACKED) {
+        // Packed layout: pair 0 already in place, pair 1 three bits low, pair 2
+        // six bits low with its signs at 13/29, pair 3 three bits high with its
+        // signs at 14/30.
+        out[0] = bf16x2_mul(q & 0x81C081C0u, f2);
+        out[1] = bf16x2_mul((q << 3) & 0x81C081C0u, f2);
+        out[2] = bf16x2_mul(((q << 6) & 0x01C001C0u) | ((q << 2) & 0x80008000u), f2);
+        out[3] = bf16x2_mul(((q >> 3) & 0x01C001C0u) | ((q << 1) & 0x80008000u), f2);
+        return;
+    }
     const uint32_t q4 = q << 4;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -154,7 +170,7 @@ __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-template <int BN>
+template <int BN, bool PACKED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap u_map, const __grid_constant__ CUtensorMap scl_map,
@@ -380,18 +396,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint4 c0 = ld_shared_v4(rb + (uint32_t)(((2 * q) ^ (row & 7)) * 16));
                     const uint4 c1 = ld_shared_v4(rb + (uint32_t)(((2 * q + 1) ^ (row & 7)) * 16));
                     const uint32_t sc = ld_shared_u32(smem_u32(R_ring + rs * RAW_STAGE + RAW_CODES) + row * 16 + q * 4);
-                    const uint32_t f0 = scale_factor_bf16x2(sc & 0xFFu, pow2);
-                    const uint32_t f1 = scale_factor_bf16x2((sc >> 8) & 0xFFu, pow2);
-                    const uint32_t f2 = scale_factor_bf16x2((sc >> 16) & 0xFFu, pow2);
-                    const uint32_t f3 = scale_factor_bf16x2(sc >> 24, pow2);
-                    dequant_word(c0.x, f0, out + 0);
-                    dequant_word(c0.y, f0, out + 4);
-                    dequant_word(c0.z, f1, out + 8);
-                    dequant_word(c0.w, f1, out + 12);
-                    dequant_word(c1.x, f2, out + 16);
-                    dequant_word(c1.y, f2, out + 20);
-                    dequant_word(c1.z, f3, out + 24);
-                    dequant_word(c1.w, f3, out + 28);
+                    const uint32_t f0 = scale_factor_bf16x2(sc << 20, pow2);
+                    const uint32_t f1 = scale_factor_bf16x2(sc << 12, pow2);
+                    const uint32_t f2 = scale_factor_bf16x2(sc << 4, pow2);
+                    const uint32_t f3 = scale_factor_bf16x2(sc >> 4, pow2);
+                    dequant_word<PACKED>(c0.x, f0, out + 0);
+                    dequant_word<PACKED>(c0.y, f0, out + 4);
+                    dequant_word<PACKED>(c0.z, f1, out + 8);
+                    dequant_word<PACKED>(c0.w, f1, out + 12);
+                    dequant_word<PACKED>(c1.x, f2, out + 16);
+                    dequant_word<PACKED>(c1.y, f2, out + 20);
+                    dequant_word<PACKED>(c1.z, f3, out + 24);
+                    dequant_word<PACKED>(c1.w, f3, out + 28);
                 } else {
                     // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
                     const int j0 = (i - n_main) * BK;
@@ -719,10 +735,10 @@ const Env &env()
 
 template <int BN>
 qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const CUtensorMap &sm,
-                       const TcFwdParams &p, unsigned grid, cudaStream_t s)
+                       const TcFwdParams &p, unsigned grid, bool packed, cudaStream_t s)
 {
-    if (cudaFuncSetAttribute(tc_fwd_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) !=
-        cudaSuccess)
+    auto kernel = packed ? tc_fwd_kernel<BN, true> : tc_fwd_kernel<BN, false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) != cudaSuccess)
         return QERL_ERR_CUDA;
     // Programmatic dependent launch: the CTAs may start while the LoRA
     // down-projection still runs and stream their (static) weights; the token
@@ -737,7 +753,7 @@ qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUten
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, tc_fwd_kernel<BN>, cm, xm, um, sm, p) != cudaSuccess) return QERL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, cm, xm, um, sm, p) != cudaSuccess) return QERL_ERR_CUDA;
     return launched();
 }
 
@@ -815,11 +831,11 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     p.fault = env().fault;
     const unsigned grid = (unsigned)(tiles * pl.splits);
     switch (pl.BN) {
-    case 16: return launch_fwd<16>(cm, xm, um, sm, p, grid, s);
-    case 32: return launch_fwd<32>(cm, xm, um, sm, p, grid, s);
-    case 64: return launch_fwd<64>(cm, xm, um, sm, p, grid, s);
-    case 128: return launch_fwd<128>(cm, xm, um, sm, p, grid, s);
-    default: return launch_fwd<256>(cm, xm, um, sm, p, grid, s);
+    case 16: return launch_fwd<16>(cm, xm, um, sm, p, grid, a.packed != 0, s);
+    case 32: return launch_fwd<32>(cm, xm, um, sm, p, grid, a.packed != 0, s);
+    case 64: return launch_fwd<64>(cm, xm, um, sm, p, grid, a.packed != 0, s);
+    case 128: return launch_fwd<128>(cm, xm, um, sm, p, grid, a.packed != 0, s);
+    default: return launch_fwd<256>(cm, xm, um, sm, p, grid, a.packed != 0, s);
     }
 }
 
