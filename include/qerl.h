@@ -183,6 +183,24 @@ qerl_status qerl_nvfp4_lora_linear_bwd(const void *dy, const void *x, int64_t M,
                                        size_t ws_bytes, qerl_stream_t stream);
 
 /*
+ * Chained launches (default on).  The kernels of consecutive calls on a stream
+ * are launched as programmatic dependents: a kernel may be scheduled before the
+ * preceding work has finished, and it waits for that work (griddepcontrol.wait)
+ * before it reads or writes memory the work touches -- with one exception: the
+ * forward's main kernel starts reading the frozen weight (codes, scales,
+ * tensor_scale) before the preceding work has finished.  Chaining hides the
+ * launch gap between calls and overlaps each forward's weight stream with the
+ * tail of the previous call.  Contract while on: a kernel that writes a
+ * forward's codes, scales or tensor_scale must have completed before that
+ * forward is enqueued, or be separated from it by any launch that does not
+ * signal programmatic completion early (every library entry point that
+ * writes weights -- quantize, pack, unpack -- is such a launch).  on = 0 turns
+ * chaining off (every kernel waits for the preceding work to complete);
+ * on = 1 turns it on; anything else returns QERL_ERR_INVALID_ARG.  Global.
+ */
+qerl_status qerl_set_launch_chaining(int on);
+
+/*
  * Packed code layout for the tensor-core dequantizer.  The pages name Marlin as
  * the kernel that serves the NVFP4 x BF16 product ("QeRL" README mirror,
  * feature list; dataforcee, RL-loop section); kernels of that family lay the

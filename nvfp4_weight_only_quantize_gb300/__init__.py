@@ -33,6 +33,7 @@ EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_lin
             "qerl_nvfp4_lora_linear_fwd_packed", "qerl_nvfp4_lora_linear_bwd_packed",
             "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_noise", "qerl_aqn_sigma",
             "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
+            "qerl_set_launch_chaining",
             "qerl_launch_count"]
 
 
@@ -84,6 +85,7 @@ def lib() -> C.CDLL:
                 "qerl_get_error": ([vp], i32),
                 "qerl_status_string": ([i32], C.c_char_p),
                 "qerl_set_linear_algo": ([i32], i32),
+                "qerl_set_launch_chaining": ([i32], i32),
                 "qerl_launch_count": ([], u64),
             }
             sig["qerl_nvfp4_lora_linear_fwd_packed"] = sig["qerl_nvfp4_lora_linear_fwd"]
@@ -125,6 +127,11 @@ def workspace(op: int, M: int, N: int, K: int, r: int, device="cuda") -> torch.T
 
 def set_linear_algo(algo: int):
     _check(lib().qerl_set_linear_algo(algo), "qerl_set_linear_algo")
+
+
+def set_launch_chaining(on: bool):
+    """Programmatic dependent launches between consecutive calls (default on)."""
+    _check(lib().qerl_set_launch_chaining(int(bool(on))), "qerl_set_launch_chaining")
 
 
 def launch_count() -> int:

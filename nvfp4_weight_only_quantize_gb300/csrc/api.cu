@@ -10,6 +10,7 @@
 namespace qerl {
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_chain{1};
 
 // First error a kernel found on this device (0 = none); cleared by qerl_get_error.
 static __device__ unsigned int g_device_error;
@@ -114,3 +115,10 @@ extern "C" float qerl_aqn_sigma(int64_t step, int64_t total_steps, float sigma_s
 }
 
 extern "C" uint64_t qerl_launch_count(void) { return g_launches.load(); }
+
+extern "C" qerl_status qerl_set_launch_chaining(int on)
+{
+    if (on != 0 && on != 1) return QERL_ERR_INVALID_ARG;
+    g_chain.store(on);
+    return QERL_OK;
+}

@@ -38,6 +38,7 @@ __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32
                                  const __nv_bfloat16 *__restrict__ gamma, float sigma, float *__restrict__ scale_out,
                                  float *__restrict__ z_out, uint64_t *__restrict__ raw_out)
 {
+    pdl_trigger();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i * 4 >= H) return;
     uint64_t w[4] = {(uint64_t)i, step, 0ull, 0ull};
@@ -53,6 +54,9 @@ __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32
         z[2 * p] = rad * cs;
         z[2 * p + 1] = rad * sn;
     }
+    // The draws need no input: only the writes (and gamma) wait for the
+    // preceding work when the launch is chained.
+    pdl_wait();
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const int64_t c = 4 * i + p;
@@ -89,6 +93,8 @@ __global__ void __launch_bounds__(kNormThreads)
                    const __nv_bfloat16 *__restrict__ gamma, float eps, __nv_bfloat16 *__restrict__ y)
 {
     __shared__ float red[32];
+    pdl_trigger();
+    pdl_wait();
     const bool vec = (H % 8) == 0;
     for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const __nv_bfloat16 *row = x + m * H;
@@ -170,14 +176,14 @@ extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, con
     if (noisy) {
         gscale = static_cast<float *>(ws);
         const int64_t n = (H + 3) / 4;
-        aqn_noise_kernel<<<(unsigned)((n + 127) / 128), 128, 0, s>>>(
-            H, seed, step, layer_id, static_cast<const __nv_bfloat16 *>(gamma), sigma, gscale, nullptr, nullptr);
-        QERL_TRY(launched());
+        QERL_TRY(launched(launch_k(aqn_noise_kernel, dim3((unsigned)((n + 127) / 128)), dim3(128), 0, s,
+                                   g_chain.load() != 0, H, seed, step, layer_id,
+                                   static_cast<const __nv_bfloat16 *>(gamma), sigma, gscale, (float *)nullptr,
+                                   (uint64_t *)nullptr)));
     }
     int64_t g = M;
     if (g > 8 * num_sms()) g = 8 * num_sms();
-    rmsnorm_kernel<<<(unsigned)g, kNormThreads, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), M, H, gscale,
-                                                         static_cast<const __nv_bfloat16 *>(gamma), eps,
-                                                         static_cast<__nv_bfloat16 *>(y));
-    return launched();
+    return launched(launch_k(rmsnorm_kernel, dim3((unsigned)g), dim3(kNormThreads), 0, s, g_chain.load() != 0,
+                             static_cast<const __nv_bfloat16 *>(x), M, H, (const float *)gscale,
+                             static_cast<const __nv_bfloat16 *>(gamma), eps, static_cast<__nv_bfloat16 *>(y)));
 }

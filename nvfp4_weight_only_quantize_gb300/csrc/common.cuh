@@ -41,10 +41,40 @@ inline int num_sms()
 }
 
 // After a launch: count it and turn a launch error into QERL_ERR_CUDA.
+// Programmatic dependent launch: when `chained`, the kernel may be scheduled
+// before the preceding work on the stream has finished; it must execute
+// pdl_wait() before it touches memory that preceding work writes or reads.
+extern std::atomic<int> g_chain;
+template <typename... Params, typename... Args>
+cudaError_t launch_k(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool chained,
+                     Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+// Wait for the preceding grid (no-op unless launched chained) / let the next
+// chained grid be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 inline qerl_status launched()
 {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return cudaPeekAtLastError() == cudaSuccess ? QERL_OK : QERL_ERR_CUDA;
+}
+inline qerl_status launched(cudaError_t e)
+{
+    if (e != cudaSuccess) return QERL_ERR_CUDA;
+    return launched();
 }
 
 #define QERL_TRY(expr)                          \

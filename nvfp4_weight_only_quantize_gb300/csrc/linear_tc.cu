@@ -104,6 +104,7 @@ struct TcFwdParams {
     unsigned int *err;
     unsigned long long timeout_ns;
     int fault;           // test hook: CTA 0 withholds one arrival so its waits time out
+    int chain;           // launched chained: token tiles and B wait for the preceding grid
 };
 
 // Exponent offset c in [7, 116] with s_t * 2^c in [1, 2) when possible: the
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_trigger();  // a chained successor may be scheduled (it waits for this grid before touching memory)
     const unsigned long long deadline = globaltimer_ns() + p.timeout_ns;
 
     // Bounded wait for the phase with this parity; false once the CTA aborts.
@@ -298,6 +300,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             int issued = 0;
+            // Chained: x may come from the work before the down-projection
+            // grid, which that grid waited for; wait for it before any x tile.
+            if (p.chain) pdl_wait();
             for (int j = 0; j < n_stages; ++j) {
                 const int slot = j & (C::XS - 1);
                 const uint32_t round = (uint32_t)(j >> C::LOG_XS);
@@ -410,6 +415,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     dequant_word<PACKED>(c1.w, f3, out + 28);
                 } else {
                     // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
+                    // (Chained: B may be written by work before this call.)
+                    if (p.chain) pdl_wait();
                     const int j0 = (i - n_main) * BK;
                     const __nv_bfloat16 *b = p.Bl + (size_t)(row_ok ? n : 0) * p.r + j0;
                     if (row_ok && (p.r & 7) == 0 && j0 + 64 <= p.r) {
@@ -574,7 +581,8 @@ __global__ void __launch_bounds__(LD_THREADS)
                      __nv_bfloat16 *__restrict__ u, uint32_t *__restrict__ counters, int n_counters)
 {
     __shared__ float red[LD_THREADS / 32][MB * JB];
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    pdl_trigger();  // the main kernel may start streaming its weight now
+    pdl_wait();     // chained launch: x, A and the counters follow the preceding work
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
     const int jgroups = r_pad / JB;
@@ -789,22 +797,25 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return QERL_ERR_CUDA;
 
-    // 1) LoRA down-projection (+ counter reset)
+    // 1) LoRA down-projection (+ counter reset).  Chained, it may start before
+    //    the preceding work finishes (it waits for it before touching memory),
+    //    and the main kernel may then stream and dequantize its (frozen) weight
+    //    while that work is still running.
+    const bool chain = g_chain.load() != 0;
     {
         if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
             constexpr int MB = 4, JB = 2;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
-            lora_down_kernel<MB, JB><<<blocks, LD_THREADS, 0, s>>>(a.x, a.A, (int)a.M, (int)a.K, a.r, pl.r_pad,
-                                                                   a.lora_scale, a.tensor_scale, a.t_out, u,
-                                                                   counters, tiles);
+            QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
+                                       a.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, a.tensor_scale,
+                                       a.t_out, u, counters, tiles)));
         } else {
             constexpr int MB = 8, JB = 4;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
-            lora_down_kernel<MB, JB><<<blocks, LD_THREADS, 0, s>>>(a.x, a.A, (int)a.M, (int)a.K, a.r, pl.r_pad,
-                                                                   a.lora_scale, a.tensor_scale, a.t_out, u,
-                                                                   counters, tiles);
+            QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
+                                       a.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, a.tensor_scale,
+                                       a.t_out, u, counters, tiles)));
         }
-        QERL_TRY(launched());
     }
 
     // 2) main tensor-core kernel
@@ -829,6 +840,7 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     p.err = error_word();
     p.timeout_ns = env().timeout_ns;
     p.fault = env().fault;
+    p.chain = chain ? 1 : 0;
     const unsigned grid = (unsigned)(tiles * pl.splits);
     switch (pl.BN) {
     case 16: return launch_fwd<16>(cm, xm, um, sm, p, grid, a.packed != 0, s);
