@@ -30,7 +30,9 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "linear.cuh"
 #include "sm100_ptx.cuh"
@@ -62,9 +64,9 @@ struct Cfg {
     // A stage holds SPS k-steps of the dequantized weight tile (TMEM); at least
     // DQ_GROUPS of them, so a group never waits on a stage two mbarrier phases
     // ahead of the MMA (parity aliasing).
-    // A stages (TMEM); a power of two: slot and phase are a mask and a shift.
-    static constexpr int S = SPS == 4 ? 2 : 4;
-    static constexpr int LOG_S = SPS == 4 ? 1 : 2;
+    // One more stage than dequant groups (where TMEM allows): a group can fill a
+    // free stage while the MMA still reads the one it filled before.
+    static constexpr int S = SPS == 4 ? 3 : 4;
     static_assert(S >= DQ_GROUPS, "parity waits need at least one stage per dequant group");
     // Token-tile stages (smem), deeper than the A ring: a token slot is reloaded
     // only after the MMA that read it completed, a ~2 us round trip.
@@ -72,7 +74,7 @@ struct Cfg {
     static constexpr int LOG_XS = BN >= 128 ? 1 : 2;
     static constexpr int R = 4;  // raw (code+scale) stages
     static_assert(GK % SPS == 0 && GK / SPS <= DQ_GROUPS, "each group has at most one stage per raw stage");
-    static_assert((1 << LOG_S) == S && (1 << LOG_XS) == XS, "power-of-two rings");
+    static_assert((1 << LOG_XS) == XS, "power-of-two token ring");
     static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
     static_assert(R * GK >= S * SPS, "raw ring deep enough for parity-safe waits");
     static constexpr int X_STEP = BN * BK * 2;
@@ -105,6 +107,8 @@ struct TcFwdParams {
     unsigned long long timeout_ns;
     int fault;           // test hook: CTA 0 withholds one arrival so its waits time out
     int chain;           // launched chained: token tiles and B wait for the preceding grid
+    int cs;              // CTAs per cluster (1, 2 or 4): consecutive weight tiles sharing one
+                         // token tile per stage, each CTA loading 1/cs of it for all (multicast)
 };
 
 // Exponent offset c in [7, 116] with s_t * 2^c in [1, 2) when possible: the
@@ -197,9 +201,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int *ep_ok = last_flag + 1;  // [4]: epilogue warps' view of acc_full
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x % p.splits;
-    const int tile = blockIdx.x / p.splits;
-    const int n_tile = tile % p.n_tiles, m_tile = tile / p.n_tiles;
+    // blockIdx.x = (split * m_tiles + m_tile) * n_tiles + n_tile; n_tiles % cs == 0, so
+    // the CTAs of a cluster share split and m_tile (the same token tiles) and the
+    // cluster rank is n_tile % cs.
+    const int cs = p.cs;
+    const uint32_t crank = cs > 1 ? cluster_ctarank() : 0u;
+    const uint16_t cmask = (uint16_t)((1u << cs) - 1u);
+    const int n_tile = blockIdx.x % p.n_tiles;
+    const int m_tile = (blockIdx.x / p.n_tiles) % p.m_tiles;
+    const int split = blockIdx.x / (p.n_tiles * p.m_tiles);
+    const int tile = m_tile * p.n_tiles + n_tile;
     const int n0 = n_tile * TILE_N, m0 = m_tile * BN;
     const int k_begin = split * p.steps_per_split;  // a multiple of GK
     const int k_end = min(p.nk, k_begin + p.steps_per_split);
@@ -210,8 +221,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int main_stages = n_main / SPS;
     // Every CTA walks its k-range from a different raw group, so that the CTAs
     // do not all read the same token tile from L2 at the same time.
-    const int grot = n_groups > 0 ? (n_tile * 5 + m_tile * 3) % n_groups : 0;
-    auto kstep = [&](int i) { return k_begin + ((i / GK + grot) % n_groups) * GK + i % GK; };
+    // The rotation is shared by each aligned group of four weight tiles (so by
+    // every cluster) and does not depend on the cluster size: the summation
+    // order, hence the result, is the same for every cluster size.
+    const int grot = n_groups > 0 ? ((n_tile >> 2) * 5 + m_tile * 3) % n_groups : 0;
+    // k-step of the CTA's i-th main step.  No division: the producers run on one
+    // lane that shares its SM sub-partition with issue-bound dequantizing warps,
+    // where every extra dependent instruction costs many cycles.
+    auto kstep = [&](int i) {
+        int gg = i / GK + grot;  // GK is a power of two
+        if (gg >= n_groups) gg -= n_groups;
+        return k_begin + gg * GK + i % GK;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::R; ++i) {
@@ -220,7 +241,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < C::XS; ++i) {
             mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], 1);
+            mbar_init(&x_empty[i], (uint32_t)cs);  // every CTA of the cluster frees the slot
         }
         for (int i = 0; i < C::S; ++i) {
             mbar_init(&a_full[i], DQ_GROUP_WARPS);
@@ -244,7 +265,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (cs > 1)
+        cluster_sync();  // every CTA's barriers are initialised before any multicast reaches them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();  // a chained successor may be scheduled (it waits for this grid before touching memory)
@@ -319,10 +343,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int sub = 0; sub < SPS; ++sub) {
                     if (sub >= nsub) break;
                     const int i = j * SPS + sub;
-                    if (i < n_main)
-                        tma_load_2d_hint(dst + sub * C::X_STEP, &x_map, &x_full[slot], kstep(i) * BK, m0, pol);
-                    else
-                        tma_load_2d_hint(dst + sub * C::X_STEP, &u_map, &x_full[slot], (i - n_main) * BK, m0, pol);
+                    const CUtensorMap *map = i < n_main ? &x_map : &u_map;
+                    const int kx = i < n_main ? kstep(i) * BK : (i - n_main) * BK;
+                    if (cs == 1)
+                        tma_load_2d_hint(dst + sub * C::X_STEP, map, &x_full[slot], kx, m0, pol);
+                    else if ((sub & (cs - 1)) == (int)crank)  // this CTA's share, to every CTA of the cluster
+                        tma_load_2d_multicast(dst + sub * C::X_STEP, map, &x_full[slot], kx, m0, cmask, pol);
                 }
                 issued = j + 1;
             }
@@ -340,7 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t at0 = tmem + (uint32_t)C::A_COL0;
         bool ready = n_stages > 0 && __all_sync(0xFFFFFFFFu, wait(&a_full[0], 0) && wait(&x_full[0], 0));
         for (int j = 0; j < n_stages && ready; ++j) {
-            const int s = j & (C::S - 1), xs = j & (C::XS - 1);
+            const int s = j % C::S, xs = j & (C::XS - 1);
             const int nsub = min(SPS, n_steps - j * SPS);
             tc_fence_after();
             if (elect_one()) {
@@ -356,12 +382,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                      (j > 0 || sub > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&stage_empty[s]);
-                umma_commit(&x_empty[xs]);
+                if (cs == 1)
+                    umma_commit(&x_empty[xs]);
+                else
+                    umma_commit_multicast(&x_empty[xs], cmask);  // the slot is free in this CTA
             }
             __syncwarp();
             if (j + 1 < n_stages) {
-                const int s1 = (j + 1) & (C::S - 1), xs1 = (j + 1) & (C::XS - 1);
-                ready = __all_sync(0xFFFFFFFFu, wait(&a_full[s1], (uint32_t)((j + 1) >> C::LOG_S) & 1u) &&
+                const int s1 = (j + 1) % C::S, xs1 = (j + 1) & (C::XS - 1);
+                ready = __all_sync(0xFFFFFFFFu, wait(&a_full[s1], (uint32_t)((j + 1) / C::S) & 1u) &&
                                                     wait(&x_full[xs1], (uint32_t)((j + 1) >> C::LOG_XS) & 1u));
             }
         }
@@ -563,6 +592,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    // No CTA leaves while a peer may still multicast into it or arrive on its barriers.
+    if (cs > 1) cluster_sync();
 }
 
 // LoRA down-projection for the tensor-core path: t = x A^T (FP32), written as
@@ -726,8 +757,11 @@ bool tc_fwd_applies(int64_t M, int64_t N, int64_t K, int r)
 struct Env {
     unsigned long long timeout_ns = 2000000000ull;  // 2 s
     int fault = 0;
+    int cluster = 0;  // QERL_TC_CLUSTER = 1, 2 or 4 forces that cluster size (tests)
     Env()
     {
+        const char *c = std::getenv("QERL_TC_CLUSTER");
+        if (c && (c[0] == '1' || c[0] == '2' || c[0] == '4') && c[1] == 0) cluster = c[0] - '0';
         const char *f = std::getenv("QERL_TEST_WITHHOLD_ARRIVAL");
         if (f && f[0] == '1') {
             fault = 1;
@@ -741,26 +775,74 @@ const Env &env()
     return e;
 }
 
+// Largest cluster size in {4, 2, 1} that divides the weight tiles and still lets
+// the whole grid be resident at once (clusters are placed within one GPC).
+template <typename Kernel>
+int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int n_tiles, unsigned grid)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> max_clusters;  // (kernel, cs) -> resident clusters
+    int forced = env().cluster;
+    for (int cs = 4; cs >= 2; cs /= 2) {
+        if (forced && cs != forced) continue;
+        if (n_tiles % cs != 0) continue;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), cs * 64 + dev);
+        int nc = 0;
+        {
+            std::lock_guard<std::mutex> lk(mu);
+            auto it = max_clusters.find(key);
+            if (it != max_clusters.end()) {
+                nc = it->second;
+            } else {
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeClusterDimension;
+                at[0].val.clusterDim.x = (unsigned)cs;
+                at[0].val.clusterDim.y = 1;
+                at[0].val.clusterDim.z = 1;
+                cfg.attrs = at;
+                cfg.numAttrs = 1;
+                cfg.gridDim = dim3((unsigned)cs);
+                if (cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg) != cudaSuccess) {
+                    cudaGetLastError();
+                    nc = 0;
+                }
+                max_clusters[key] = nc;
+            }
+        }
+        if (forced || (unsigned)(nc * cs) >= grid) return cs;
+    }
+    return 1;
+}
+
 template <int BN>
 qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const CUtensorMap &sm,
-                       const TcFwdParams &p, unsigned grid, bool packed, cudaStream_t s)
+                       const TcFwdParams &p0, unsigned grid, bool packed, cudaStream_t s)
 {
     auto kernel = packed ? tc_fwd_kernel<BN, true> : tc_fwd_kernel<BN, false>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) != cudaSuccess)
         return QERL_ERR_CUDA;
-    // Programmatic dependent launch: the CTAs may start while the LoRA
-    // down-projection still runs and stream their (static) weights; the token
-    // producer waits for it with griddepcontrol.wait.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    TcFwdParams p = p0;
+    p.cs = pick_cluster(kernel, cfg, p.n_tiles, grid);
+    // Programmatic dependent launch: the CTAs may start while the LoRA
+    // down-projection still runs and stream their (static) weights; the token
+    // producer waits for it with griddepcontrol.wait.  Clusters of p.cs CTAs
+    // share the token tiles (multicast).
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, cm, xm, um, sm, p) != cudaSuccess) return QERL_ERR_CUDA;
     return launched();
 }
