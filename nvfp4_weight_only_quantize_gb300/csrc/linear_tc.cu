@@ -777,12 +777,13 @@ const Env &env()
 
 // Largest cluster size in {4, 2, 1} that divides the weight tiles and still lets
 // the whole grid be resident at once (clusters are placed within one GPC).
-template <typename Kernel>
+template <bool MULTICAST, typename Kernel>
 int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int n_tiles, unsigned grid)
 {
     static std::mutex mu;
     static std::map<std::pair<const void *, int>, int> max_clusters;  // (kernel, cs) -> resident clusters
     int forced = env().cluster;
+    if (!forced && !MULTICAST) return 1;
     for (int cs = 4; cs >= 2; cs /= 2) {
         if (forced && cs != forced) continue;
         if (n_tiles % cs != 0) continue;
@@ -829,7 +830,9 @@ qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUten
     cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
     cfg.stream = s;
     TcFwdParams p = p0;
-    p.cs = pick_cluster(kernel, cfg, p.n_tiles, grid);
+    // Decode-sized token tiles are cheap to load per CTA, and clusters would tie
+    // the CTAs' pipelines together; wide (prefill) tiles share them.
+    p.cs = pick_cluster<(BN >= 256)>(kernel, cfg, p.n_tiles, grid);
     // Programmatic dependent launch: the CTAs may start while the LoRA
     // down-projection still runs and stream their (static) weights; the token
     // producer waits for it with griddepcontrol.wait.  Clusters of p.cs CTAs
