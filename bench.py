@@ -428,7 +428,10 @@ def other_rows(dev):
                    warm=1)
     fl = 2.0 * M * N * K + 2.0 * M * wl.r * (3 * N + 2 * K)
     rows["a5_backward"] = {"workload": f"qwen2.5-7b {name} {N}x{K}, M={M}, r={wl.r}", "us": round(sec * 1e6, 1),
-                           "TFLOPs": round(fl / sec / 1e12, 2), "path": "CUDA cores (tiled SIMT GEMMs)"}
+                           "TFLOPs": round(fl / sec / 1e12, 2),
+                           "frac_of_bf16_peak": round(fl / sec / 1e12 / bf16, 3),
+                           "path": "dx on tensor cores (tcgen05, transposed dequant); v, t, dA, dB on CUDA cores "
+                                   "(thin rank-r products, split over the reduction)"}
     torch.cuda.synchronize()
     return rows
 

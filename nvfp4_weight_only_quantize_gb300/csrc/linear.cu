@@ -8,6 +8,7 @@
 // epilogue.  Backward with the weight frozen:
 //   v = dy * B,  dx = s_t * dy * w' + s * v * A,  dA = s * v^T * x,
 //   dB = s * dy^T * (x * A^T).
+#include <algorithm>
 #include <atomic>
 
 #include "linear.cuh"
@@ -20,16 +21,30 @@ std::atomic<int> g_algo{QERL_ALGO_AUTO};
 
 // ------------------------------------------------------------ operand loaders
 struct RowBF16 {  // (p, k) -> base[p * ld + k]
+    static constexpr bool kVec8 = true;  // 8 consecutive k in one 16-byte load
     const __nv_bfloat16 *base;
     int64_t ld;
     __device__ float operator()(int64_t p, int64_t k) const { return bf16f(base[p * ld + k]); }
+    __device__ bool vec_ok() const { return (ld & 7) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0; }
+    __device__ uint4 load8(int64_t p, int64_t k) const
+    {
+        return __ldg(reinterpret_cast<const uint4 *>(base + p * ld + k));
+    }
 };
 struct ColBF16 {  // (p, k) -> base[k * ld + p]
+    static constexpr bool kColMajor = true;
+    static constexpr bool kVec8 = true;  // 8 consecutive p in one 16-byte load
     const __nv_bfloat16 *base;
     int64_t ld;
     __device__ float operator()(int64_t p, int64_t k) const { return bf16f(base[k * ld + p]); }
+    __device__ bool vec_ok() const { return (ld & 7) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0; }
+    __device__ uint4 load8(int64_t p, int64_t k) const
+    {
+        return __ldg(reinterpret_cast<const uint4 *>(base + k * ld + p));
+    }
 };
 struct ColF32 {  // (p, k) -> base[k * ld + p]
+    static constexpr bool kColMajor = true;
     const float *base;
     int64_t ld;
     __device__ float operator()(int64_t p, int64_t k) const { return base[k * ld + p]; }
@@ -55,6 +70,7 @@ struct WRow {  // (n, k)
     __device__ float operator()(int64_t n, int64_t k) const { return wprime(codes, scales, K, n, k, packed); }
 };
 struct WCol {  // (k, n)
+    static constexpr bool kColMajor = true;
     const uint8_t *codes, *scales;
     int64_t K;
     int packed;
@@ -67,7 +83,7 @@ struct StoreF32 {  // out[p, q] = (accumulate ? out : 0) + alpha * v
     int64_t ld;
     float alpha;
     int accumulate;
-    __device__ void operator()(int64_t p, int64_t q, float v) const
+    __device__ void operator()(int64_t p, int64_t q, float v, int) const
     {
         float *o = out + p * ld + q;
         *o = accumulate ? fmaf(alpha, v, *o) : alpha * v;
@@ -82,7 +98,7 @@ struct FwdEpi {
     const __nv_bfloat16 *B;
     int r;
     float s;
-    __device__ void operator()(int64_t m, int64_t n, float acc) const
+    __device__ void operator()(int64_t m, int64_t n, float acc, int) const
     {
         float l = 0.0f;
         for (int j = 0; j < r; ++j) l = fmaf(t[m * r + j], bf16f(B[n * r + j]), l);
@@ -98,7 +114,7 @@ struct DxEpi {
     const __nv_bfloat16 *A;
     int r;
     float s;
-    __device__ void operator()(int64_t m, int64_t k, float acc) const
+    __device__ void operator()(int64_t m, int64_t k, float acc, int) const
     {
         float l = 0.0f;
         for (int j = 0; j < r; ++j) l = fmaf(v[m * r + j], bf16f(A[(int64_t)j * K + k]), l);
@@ -106,27 +122,102 @@ struct DxEpi {
     }
 };
 
-// C[p, q] = sum_k L(p, k) * R(q, k), 64x64 tiles, 16-deep k steps staged in
-// shared memory as FP32, 4x4 outputs per thread.  Bounds-checked everywhere.
+// Operands contiguous along p (rather than k) are staged with consecutive
+// threads on consecutive p, so that their loads coalesce.
+template <class T, class = void>
+struct col_major {
+    static constexpr bool value = false;
+};
+template <class T>
+struct col_major<T, decltype((void)T::kColMajor)> {
+    static constexpr bool value = T::kColMajor;
+};
+
+template <class T, class = void>
+struct vec8 {
+    static constexpr bool value = false;
+};
+template <class T>
+struct vec8<T, decltype((void)T::kVec8)> {
+    static constexpr bool value = T::kVec8;
+};
+
+__device__ __forceinline__ void unpack8(uint4 u, float *f)
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        f[2 * e] = __uint_as_float(w[e] << 16);
+        f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
+
+template <class L>
+__device__ __forceinline__ void stage16(float (&S)[16][68], const L &ld, int tid, int64_t p0, int64_t P, int64_t k0,
+                                        int64_t kend)
+{
+    if constexpr (vec8<L>::value) {
+        // A 64 x 16 block as 128 16-byte loads, one per thread of the first half;
+        // rows past P read as zeros (for p-contiguous operands P % 8 == 0, so a
+        // vector never straddles P).
+        if (ld.vec_ok() && k0 + 16 <= kend && (!col_major<L>::value || (P & 7) == 0)) {
+            if (tid < 128) {
+                float f[8];
+                if (col_major<L>::value) {  // 8 p at one k
+                    const int kk = tid >> 3, pp = (tid & 7) * 8;
+                    if (p0 + pp < P) {
+                        unpack8(ld.load8(p0 + pp, k0 + kk), f);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) S[kk][pp + e] = f[e];
+                } else {  // 8 k at one p
+                    const int pp = tid >> 1, kk = (tid & 1) * 8;
+                    if (p0 + pp < P) {
+                        unpack8(ld.load8(p0 + pp, k0 + kk), f);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) S[kk + e][pp] = f[e];
+                }
+            }
+            return;
+        }
+    }
+    for (int i = tid; i < 1024; i += 256) {
+        const int pp = col_major<L>::value ? (i & 63) : (i >> 4);
+        const int kk = col_major<L>::value ? (i >> 6) : (i & 15);
+        const int64_t k = k0 + kk, p = p0 + pp;
+        S[kk][pp] = (p < P && k < kend) ? ld(p, k) : 0.0f;
+    }
+}
+
+// C[p, q] = sum_k L(p, k) * R(q, k) over k in [kbeg, kend) with kbeg, kend from
+// blockIdx.z (split k: each split writes its own partial), 64x64 tiles,
+// 16-deep k steps staged in shared memory as FP32, 4x4 outputs per thread.
+// Bounds-checked everywhere.
 template <class LL, class LR, class EP>
-__global__ void __launch_bounds__(256) simt_gemm(int64_t P, int64_t Q, int64_t Kd, LL lo, LR ro, EP ep)
+__global__ void __launch_bounds__(256) simt_gemm(int64_t P, int64_t Q, int64_t Kd, int64_t kchunk, LL lo, LR ro,
+                                                 EP ep)
 {
     __shared__ float Ls[16][68];
     __shared__ float Rs[16][68];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int64_t p0 = (int64_t)blockIdx.y * 64, q0 = (int64_t)blockIdx.x * 64;
+    const int64_t kbeg = (int64_t)blockIdx.z * kchunk;
+    const int64_t kend = kbeg + kchunk < Kd ? kbeg + kchunk : Kd;
     float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-    for (int64_t k0 = 0; k0 < Kd; k0 += 16) {
-        for (int i = tid; i < 1024; i += 256) {
-            const int pp = i >> 4, kk = i & 15;
-            const int64_t k = k0 + kk, p = p0 + pp, q = q0 + pp;
-            Ls[kk][pp] = (p < P && k < Kd) ? lo(p, k) : 0.0f;
-            Rs[kk][pp] = (q < Q && k < Kd) ? ro(q, k) : 0.0f;
-        }
+    for (int64_t k0 = kbeg; k0 < kend; k0 += 16) {
+        stage16(Ls, lo, tid, p0, P, k0, kend);
+        stage16(Rs, ro, tid, q0, Q, k0, kend);
         __syncthreads();
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
@@ -147,8 +238,27 @@ __global__ void __launch_bounds__(256) simt_gemm(int64_t P, int64_t Q, int64_t K
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t p = p0 + ty + 16 * i, q = q0 + tx + 16 * j;
-            if (p < P && q < Q) ep(p, q, acc[i][j]);
+            if (p < P && q < Q) ep(p, q, acc[i][j], (int)blockIdx.z);
         }
+}
+
+// Split-k partial: part[z][p][q] = acc.
+struct PartialEpi {
+    float *part;
+    int64_t P, Q;
+    __device__ void operator()(int64_t p, int64_t q, float v, int z) const { part[(z * P + p) * Q + q] = v; }
+};
+// Sum of the partials in split order (deterministic), then StoreF32's update.
+__global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ part, int splits, int64_t P, int64_t Q,
+                                                    float *out, int64_t ld, float alpha, int accumulate)
+{
+    const int64_t n = P * Q;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float v = 0.0f;
+        for (int z = 0; z < splits; ++z) v += part[z * n + i];
+        float *o = out + (i / Q) * ld + (i % Q);
+        *o = accumulate ? fmaf(alpha, v, *o) : alpha * v;
+    }
 }
 
 template <class LL, class LR, class EP>
@@ -157,7 +267,43 @@ qerl_status run_gemm(int64_t P, int64_t Q, int64_t Kd, LL lo, LR ro, EP ep, cuda
     if (P <= 0 || Q <= 0) return QERL_OK;
     const dim3 grid((unsigned)((Q + 63) / 64), (unsigned)((P + 63) / 64));
     if (grid.y > 65535u) return QERL_ERR_SHAPE;
-    simt_gemm<<<grid, 256, 0, s>>>(P, Q, Kd, lo, ro, ep);
+    simt_gemm<<<grid, 256, 0, s>>>(P, Q, Kd, Kd > 0 ? Kd : 1, lo, ro, ep);
+    return launched();
+}
+
+// Split count for a StoreF32 product: enough 64x64 tiles x splits to fill the
+// GPU twice over, at least 512 k per split, at most 32 splits.
+int gemm_splits(int64_t P, int64_t Q, int64_t Kd)
+{
+    const int64_t tiles = ((P + 63) / 64) * ((Q + 63) / 64);
+    int64_t sp = (2 * (int64_t)num_sms() + tiles - 1) / tiles;
+    const int64_t kmax = Kd / 512;
+    if (sp > kmax) sp = kmax;
+    if (sp > 32) sp = 32;
+    return sp < 1 ? 1 : (int)sp;
+}
+size_t gemm_split_ws(int64_t P, int64_t Q, int64_t Kd)
+{
+    const int sp = gemm_splits(P, Q, Kd);
+    return sp > 1 ? round256(size_t(sp) * P * Q * sizeof(float)) : 0;
+}
+
+// C = StoreF32(sum_k L R) with k split over CTAs when the output is thin;
+// part holds gemm_split_ws(P, Q, Kd) bytes.
+template <class LL, class LR>
+qerl_status run_gemm_store(int64_t P, int64_t Q, int64_t Kd, LL lo, LR ro, StoreF32 ep, float *part, cudaStream_t s)
+{
+    const int sp = gemm_splits(P, Q, Kd);
+    if (sp == 1 || P <= 0 || Q <= 0) return run_gemm(P, Q, Kd, lo, ro, ep, s);
+    const int64_t kchunk = ((Kd + sp - 1) / sp + 15) / 16 * 16;
+    const int splits = (int)((Kd + kchunk - 1) / kchunk);
+    const dim3 grid((unsigned)((Q + 63) / 64), (unsigned)((P + 63) / 64), (unsigned)splits);
+    if (grid.y > 65535u) return QERL_ERR_SHAPE;
+    simt_gemm<<<grid, 256, 0, s>>>(P, Q, Kd, kchunk, lo, ro, PartialEpi{part, P, Q});
+    QERL_TRY(launched());
+    int64_t g = (P * Q + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    split_reduce<<<(unsigned)g, 256, 0, s>>>(part, splits, P, Q, ep.out, ep.ld, ep.alpha, ep.accumulate);
     return launched();
 }
 
@@ -169,25 +315,306 @@ qerl_status simt_fwd(const FwdArgs &a, char *ws, cudaStream_t s)
                     FwdEpi{a.y, a.N, a.tensor_scale, t, a.B, a.r, a.lora_scale}, s);
 }
 
-qerl_status simt_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
+// ------------------------------------------------------------ thin products
+// The LoRA products of the backward have one side of width r <= 64 and a long
+// reduction; they are HBM-bound.  Two CUDA-core kernels, split over the
+// reduction (partials summed in split order by split_reduce):
+//   rows x rank:   P[z][m][j] = sum_{k in split z} X[m, k] * W(k, j)
+//                  X bf16 [M, Kd] row-major; W(k, j) = Wkj[k * r + j] or Wjk[j * Kd + k]
+//   wide x rank:   P[z][w][j] (or [j][w]) = sum_{m in split z} D[m, w] * T[m, j]
+//                  D bf16 [M, Wd] row-major; T FP32 [M, r] row-major
+constexpr int THIN_TK = 32;  // reduction depth per staged chunk
+// rows (or wide columns) per CTA: 256 threads x 4 rows over r_pad / 8 rank groups
+template <int R_PAD>
+constexpr int thin_tr() { return 256 * 4 / (R_PAD / 8); }
+
+// thin_tr<R_PAD>() rows x R_PAD (32 or 64) outputs per CTA; thread = 4 rows x 8 ranks.
+template <bool WJK, int R_PAD>
+__global__ void __launch_bounds__(256) thin_rows_kernel(const __nv_bfloat16 *__restrict__ X, int64_t M, int64_t Kd,
+                                                        const __nv_bfloat16 *__restrict__ W, int r, int64_t kchunk,
+                                                        float *__restrict__ part)
 {
+    constexpr int THIN_TR = thin_tr<R_PAD>(), r_pad = R_PAD;
+    __shared__ __align__(16) __nv_bfloat16 Xs[THIN_TR][THIN_TK + 8];
+    __shared__ __align__(16) float Ws[THIN_TK][68];
+    const int tid = threadIdx.x;
+    const int jg = tid % (r_pad / 8), rg = tid / (r_pad / 8);  // rank group (8), row group (4)
+    const bool active = rg < THIN_TR / 4;
+    const int64_t m0 = (int64_t)blockIdx.x * THIN_TR;
+    const int64_t kbeg = (int64_t)blockIdx.y * kchunk;
+    const int64_t kend = kbeg + kchunk < Kd ? kbeg + kchunk : Kd;
+    float acc[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
+    for (int64_t k0 = kbeg; k0 < kend; k0 += THIN_TK) {
+        // X: 128 rows x 32 k = 512 16-byte vectors (Kd % 8 == 0, chunks of 32 k)
+        for (int v = tid; v < THIN_TR * (THIN_TK / 8); v += 256) {
+            const int row = v / (THIN_TK / 8), kk = (v % (THIN_TK / 8)) * 8;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (m0 + row < M && k0 + kk < kend) u = __ldg(reinterpret_cast<const uint4 *>(X + (m0 + row) * Kd + k0 + kk));
+            *reinterpret_cast<uint4 *>(&Xs[row][kk]) = u;
+        }
+        // W: 32 k x r_pad ranks as FP32 (zeros past r and kend)
+        for (int i = tid; i < THIN_TK * 64; i += 256) {
+            const int kk = WJK ? (i % THIN_TK) : (i / 64), j = WJK ? (i / THIN_TK) : (i % 64);
+            float w = 0.0f;
+            if (j < r && k0 + kk < kend) w = bf16f(WJK ? W[(int64_t)j * Kd + k0 + kk] : W[(k0 + kk) * r + j]);
+            Ws[kk][j] = w;
+        }
+        __syncthreads();
+        if (active) {
+#pragma unroll
+            for (int kk = 0; kk < THIN_TK; kk += 8) {
+                float xv[4][8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(&Xs[rg * 4 + i][kk]);
+                    unpack8(u, xv[i]);
+                }
+#pragma unroll
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const float4 w0 = *reinterpret_cast<const float4 *>(&Ws[kk + k8][jg * 8]);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(&Ws[kk + k8][jg * 8 + 4]);
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(xv[i][k8], wv[e], acc[i][e]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (!active) return;
+    float *out = part + (int64_t)blockIdx.y * M * r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + rg * 4 + i;
+        if (m >= M) continue;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (jg * 8 + e < r) out[m * r + jg * 8 + e] = acc[i][e];
+    }
+}
+
+// thin_tr<R_PAD>() wide columns x R_PAD ranks per CTA; thread = 4 wide x 8
+// ranks.  Output partial [w][j] (WJ) or [j][w].
+template <bool WJ, int R_PAD>
+__global__ void __launch_bounds__(256) thin_wide_kernel(const __nv_bfloat16 *__restrict__ D, int64_t M, int64_t Wd,
+                                                        const float *__restrict__ T, int r, int64_t mchunk,
+                                                        float *__restrict__ part)
+{
+    constexpr int THIN_TR = thin_tr<R_PAD>(), r_pad = R_PAD;
+    __shared__ __align__(16) __nv_bfloat16 Ds[THIN_TK][THIN_TR + 8];
+    __shared__ __align__(16) float Ts[THIN_TK][68];
+    const int tid = threadIdx.x;
+    const int jg = tid % (r_pad / 8), wg = tid / (r_pad / 8);
+    const bool active = wg < THIN_TR / 4;
+    const int64_t w0 = (int64_t)blockIdx.x * THIN_TR;
+    const int64_t mbeg = (int64_t)blockIdx.y * mchunk;
+    const int64_t mend = mbeg + mchunk < M ? mbeg + mchunk : M;
+    float acc[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
+    for (int64_t mm0 = mbeg; mm0 < mend; mm0 += THIN_TK) {
+        // D: 32 m x 128 w = 512 16-byte vectors (Wd % 8 == 0)
+        for (int v = tid; v < THIN_TK * (THIN_TR / 8); v += 256) {
+            const int mm = v / (THIN_TR / 8), ww = (v % (THIN_TR / 8)) * 8;
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (mm0 + mm < mend && w0 + ww < Wd) u = __ldg(reinterpret_cast<const uint4 *>(D + (mm0 + mm) * Wd + w0 + ww));
+            *reinterpret_cast<uint4 *>(&Ds[mm][ww]) = u;
+        }
+        for (int i = tid; i < THIN_TK * 64; i += 256) {
+            const int mm = i / 64, j = i % 64;
+            Ts[mm][j] = (j < r && mm0 + mm < mend) ? T[(mm0 + mm) * r + j] : 0.0f;
+        }
+        __syncthreads();
+        if (active) {
+#pragma unroll 8
+            for (int mm = 0; mm < THIN_TK; ++mm) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(&Ds[mm][wg * 4]);
+                const float dv[4] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+                const float4 t0 = *reinterpret_cast<const float4 *>(&Ts[mm][jg * 8]);
+                const float4 t1 = *reinterpret_cast<const float4 *>(&Ts[mm][jg * 8 + 4]);
+                const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(dv[i], tv[e], acc[i][e]);
+            }
+        }
+        __syncthreads();
+    }
+    if (!active) return;
+    float *out = part + (int64_t)blockIdx.y * Wd * r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t w = w0 + wg * 4 + i;
+        if (w >= Wd) continue;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = jg * 8 + e;
+            if (j < r) out[WJ ? w * r + j : (int64_t)j * Wd + w] = acc[i][e];
+        }
+    }
+}
+
+// Splits of a thin product with `tiles` CTAs per split over a reduction of
+// length L: fill the GPU about twice, at least 256 per split, at most 64 splits.
+int thin_splits(int64_t tiles, int64_t L)
+{
+    int64_t sp = (2 * (int64_t)num_sms() + tiles - 1) / tiles;
+    const int64_t lmax = L / 256;
+    if (sp > lmax) sp = lmax;
+    if (sp > 64) sp = 64;
+    return sp < 1 ? 1 : (int)sp;
+}
+bool thin_ok(int64_t Kd_or_wd, int r) { return r <= 64 && (Kd_or_wd % 8) == 0; }
+
+// out = alpha * X W (+ out if accumulate) over ranks: rows x rank product.
+qerl_status thin_rows(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const __nv_bfloat16 *W, bool wjk, int r,
+                      StoreF32 ep, float *part, cudaStream_t s)
+{
+    const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
+    const int64_t tiles = (M + tr - 1) / tr;
+    const int sp = thin_splits(tiles, Kd);
+    const int64_t kchunk = ((Kd + sp - 1) / sp + THIN_TK - 1) / THIN_TK * THIN_TK;
+    const int splits = (int)((Kd + kchunk - 1) / kchunk);
+    const dim3 grid((unsigned)tiles, (unsigned)splits);
+    if (r <= 32) {
+        if (wjk)
+            thin_rows_kernel<true, 32><<<grid, 256, 0, s>>>(X, M, Kd, W, r, kchunk, part);
+        else
+            thin_rows_kernel<false, 32><<<grid, 256, 0, s>>>(X, M, Kd, W, r, kchunk, part);
+    } else {
+        if (wjk)
+            thin_rows_kernel<true, 64><<<grid, 256, 0, s>>>(X, M, Kd, W, r, kchunk, part);
+        else
+            thin_rows_kernel<false, 64><<<grid, 256, 0, s>>>(X, M, Kd, W, r, kchunk, part);
+    }
+    QERL_TRY(launched());
+    int64_t g = (M * r + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    split_reduce<<<(unsigned)g, 256, 0, s>>>(part, splits, M, r, ep.out, ep.ld, ep.alpha, ep.accumulate);
+    return launched();
+}
+
+// out = alpha * D^T T (+ out): [Wd x r] when wj, else [r x Wd].
+qerl_status thin_wide(const __nv_bfloat16 *D, int64_t M, int64_t Wd, const float *T, int r, bool wj, StoreF32 ep,
+                      float *part, cudaStream_t s)
+{
+    const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
+    const int64_t tiles = (Wd + tr - 1) / tr;
+    const int sp = thin_splits(tiles, M);
+    const int64_t mchunk = ((M + sp - 1) / sp + THIN_TK - 1) / THIN_TK * THIN_TK;
+    const int splits = (int)((M + mchunk - 1) / mchunk);
+    const dim3 grid((unsigned)tiles, (unsigned)splits);
+    if (r <= 32) {
+        if (wj)
+            thin_wide_kernel<true, 32><<<grid, 256, 0, s>>>(D, M, Wd, T, r, mchunk, part);
+        else
+            thin_wide_kernel<false, 32><<<grid, 256, 0, s>>>(D, M, Wd, T, r, mchunk, part);
+    } else {
+        if (wj)
+            thin_wide_kernel<true, 64><<<grid, 256, 0, s>>>(D, M, Wd, T, r, mchunk, part);
+        else
+            thin_wide_kernel<false, 64><<<grid, 256, 0, s>>>(D, M, Wd, T, r, mchunk, part);
+    }
+    QERL_TRY(launched());
+    const int64_t P = wj ? Wd : r, Q = wj ? r : Wd;
+    int64_t g = (P * Q + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    split_reduce<<<(unsigned)g, 256, 0, s>>>(part, splits, P, Q, ep.out, ep.ld, ep.alpha, ep.accumulate);
+    return launched();
+}
+size_t thin_rows_ws(int64_t M, int64_t Kd, int r)
+{
+    const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
+    return round256(size_t(thin_splits((M + tr - 1) / tr, Kd)) * M * r * sizeof(float));
+}
+size_t thin_wide_ws(int64_t M, int64_t Wd, int r)
+{
+    const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
+    return round256(size_t(thin_splits((Wd + tr - 1) / tr, M)) * Wd * r * sizeof(float));
+}
+
+// Scratch of the backward: v, t (when not saved), v' for the tensor-core dx,
+// and the split-k partials of the thin products.
+struct BwdWs {
+    size_t vbytes, vp_bytes, part_bytes;
+};
+BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
+{
+    BwdWs w;
+    w.vbytes = round256(size_t(M) * r * sizeof(float));
+    w.vp_bytes = tc_dx_ws_bytes(M, r);
+    size_t pb = gemm_split_ws(M, r, N);                               // v = dy B
+    pb = std::max(pb, gemm_split_ws(M, r, K));                         // t = x A^T
+    pb = std::max(pb, gemm_split_ws(r, K, M));                         // dA
+    pb = std::max(pb, gemm_split_ws(N, r, M));                         // dB
+    if (thin_ok(N, r) && thin_ok(K, r)) {
+        pb = std::max(pb, thin_rows_ws(M, N, r));
+        pb = std::max(pb, thin_rows_ws(M, K, r));
+        pb = std::max(pb, thin_wide_ws(M, K, r));
+        pb = std::max(pb, thin_wide_ws(M, N, r));
+    }
+    w.part_bytes = pb;
+    return w;
+}
+
+// v = dy B, dx (tensor cores where the shape allows, else CUDA cores), then
+// dA = s v^T x and dB = s dy^T t on CUDA cores (thin, HBM-bound products,
+// split over k when their outputs are too small to fill the GPU).
+qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
+{
+    const BwdWs w = bwd_ws(a.M, a.N, a.K, a.r);
     float *v = reinterpret_cast<float *>(ws);
-    float *u = reinterpret_cast<float *>(ws + round256(size_t(a.M) * a.r * sizeof(float)));
-    QERL_TRY(run_gemm(a.M, a.r, a.N, RowBF16{a.dy, a.N}, ColBF16{a.B, a.r}, StoreF32{v, a.r, 1.0f, 0}, s));
-    if (a.dx)
-        QERL_TRY(run_gemm(a.M, a.K, a.N, RowBF16{a.dy, a.N}, WCol{a.codes, a.scales, a.K, a.packed},
-                          DxEpi{a.dx, a.K, a.tensor_scale, v, a.A, a.r, a.lora_scale}, s));
-    if (a.dA)
-        QERL_TRY(run_gemm((int64_t)a.r, a.K, a.M, ColF32{v, a.r}, ColBF16{a.x, a.K},
-                          StoreF32{a.dA, a.K, a.lora_scale, a.accumulate}, s));
+    float *u = reinterpret_cast<float *>(ws + w.vbytes);
+    char *vp = ws + 2 * w.vbytes;
+    float *part = reinterpret_cast<float *>(vp + w.vp_bytes);
+    // the thin products take the dedicated kernels when every operand is a
+    // whole number of 16-byte vectors
+    const bool thin = thin_ok(a.N, a.r) && thin_ok(a.K, a.r) && aligned16(a.dy) && aligned16(a.x) &&
+                      aligned16(a.A) && aligned16(a.B);
+    if (thin)
+        QERL_TRY(thin_rows(a.dy, a.M, a.N, a.B, false, a.r, StoreF32{v, a.r, 1.0f, 0}, part, s));
+    else
+        QERL_TRY(run_gemm_store(a.M, a.r, a.N, RowBF16{a.dy, a.N}, ColBF16{a.B, a.r}, StoreF32{v, a.r, 1.0f, 0},
+                                part, s));
+    if (a.dx) {
+        if (g_algo.load() != QERL_ALGO_SIMT && tc_dx_applies(a.M, a.N, a.K, a.r))
+            QERL_TRY(tc_dx(a, v, vp, s));
+        else
+            QERL_TRY(run_gemm(a.M, a.K, a.N, RowBF16{a.dy, a.N}, WCol{a.codes, a.scales, a.K, a.packed},
+                              DxEpi{a.dx, a.K, a.tensor_scale, v, a.A, a.r, a.lora_scale}, s));
+    }
+    if (a.dA) {
+        const StoreF32 ep{a.dA, a.K, a.lora_scale, a.accumulate};
+        if (thin)
+            QERL_TRY(thin_wide(a.x, a.M, a.K, v, a.r, false, ep, part, s));
+        else
+            QERL_TRY(run_gemm_store((int64_t)a.r, a.K, a.M, ColF32{v, a.r}, ColBF16{a.x, a.K}, ep, part, s));
+    }
     if (a.dB) {
         const float *uu = a.t_saved;
         if (!uu) {
-            QERL_TRY(run_gemm(a.M, a.r, a.K, RowBF16{a.x, a.K}, RowBF16{a.A, a.K}, StoreF32{u, a.r, 1.0f, 0}, s));
+            if (thin)
+                QERL_TRY(thin_rows(a.x, a.M, a.K, a.A, true, a.r, StoreF32{u, a.r, 1.0f, 0}, part, s));
+            else
+                QERL_TRY(run_gemm_store(a.M, a.r, a.K, RowBF16{a.x, a.K}, RowBF16{a.A, a.K},
+                                        StoreF32{u, a.r, 1.0f, 0}, part, s));
             uu = u;
         }
-        QERL_TRY(run_gemm(a.N, (int64_t)a.r, a.M, ColBF16{a.dy, a.N}, ColF32{uu, a.r},
-                          StoreF32{a.dB, a.r, a.lora_scale, a.accumulate}, s));
+        const StoreF32 ep{a.dB, a.r, a.lora_scale, a.accumulate};
+        if (thin)
+            QERL_TRY(thin_wide(a.dy, a.M, a.N, uu, a.r, true, ep, part, s));
+        else
+            QERL_TRY(run_gemm_store(a.N, (int64_t)a.r, a.M, ColBF16{a.dy, a.N}, ColF32{uu, a.r}, ep, part, s));
     }
     return QERL_OK;
 }
@@ -213,9 +640,8 @@ size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 
 size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {
-    const size_t simt = 2 * round256(size_t(M) * r * sizeof(float));
-    const size_t tc = tc_bwd_ws_bytes(M, N, K, r);
-    return simt > tc ? simt : tc;
+    const BwdWs w = bwd_ws(M, N, K, r);
+    return 2 * w.vbytes + w.vp_bytes + w.part_bytes;
 }
 
 qerl_status linear_fwd_fixed_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
@@ -300,12 +726,7 @@ qerl_status bwd_entry(const void *dy, const void *x, int64_t M, int64_t K, int64
                     scales, tensor_scale, static_cast<const __nv_bfloat16 *>(A),
                     static_cast<const __nv_bfloat16 *>(B), r, lora_scale, t_saved,
                     static_cast<__nv_bfloat16 *>(dx), dA, dB, accumulate_grads, packed};
-    cudaStream_t s = as_cuda(stream);
-    if (g_algo.load() != QERL_ALGO_SIMT) {
-        const qerl_status st = tc_linear_bwd(a, static_cast<char *>(ws), ws_bytes, s);
-        if (st != QERL_ERR_SHAPE) return st;
-    }
-    return simt_bwd(a, static_cast<char *>(ws), s);
+    return run_bwd(a, static_cast<char *>(ws), as_cuda(stream));
 }
 
 }  // namespace

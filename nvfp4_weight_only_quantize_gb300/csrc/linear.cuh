@@ -1,6 +1,8 @@
 // Internal interface between the linear entry points and their kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace qerl {
@@ -40,11 +42,21 @@ size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 // Tensor-core (tcgen05) path.  Returns QERL_ERR_SHAPE, having launched nothing,
 // when it does not cover the call; the caller then runs the CUDA-core path.
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
-size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s);
-qerl_status tc_linear_bwd(const BwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s);
 
 inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// 2-D row-major TMA tensor map: `inner` elements per row (contiguous), `outer`
+// rows of `row_bytes`; false if the driver rejects it.
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
+// Tensor-core input gradient dx = dy w_hat + s v A for the shapes it covers
+// (K % 256 == 0, N % 64 == 0, r <= 256); v = dy B in FP32 [M, r] is given, and
+// vp_ws holds tc_dx_ws_bytes(M, r) bytes of scratch.
+bool tc_dx_applies(int64_t M, int64_t N, int64_t K, int r);
+size_t tc_dx_ws_bytes(int64_t M, int r);
+qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, cudaStream_t s);
 
 // Forward with a fixed scratch buffer: validates the arguments like the
 // workspace entry point, returns QERL_ERR_TOO_LARGE when the call needs more

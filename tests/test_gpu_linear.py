@@ -67,7 +67,8 @@ def test_config0_full(algo):
 
 @pytest.mark.parametrize("M,K,N,r", [(1, 16, 1, 1), (3, 48, 33, 5), (17, 256, 200, 8), (64, 1024, 384, 32),
                                      (130, 512, 136, 16), (257, 2048, 520, 64), (9, 4096, 128, 256),
-                                     (20, 192, 100, 4), (70, 320, 257, 12)])
+                                     (20, 192, 100, 4), (70, 320, 257, 12), (200, 768, 192, 24), (129, 256, 64, 256),
+                                     (5, 512, 128, 64)])
 def test_ragged_shapes(algo, M, K, N, r):
     c = LinearCase(M, K, N, r, config=9, idx=M + N).quantize_gpu()
     _fwd_check(c)

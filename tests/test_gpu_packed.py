@@ -107,7 +107,7 @@ def test_forward_packed_qwen7b_decode_full_size(lin):
     assert_rel_rms(f64(y)[rows], ref, LIN_TOL, "y")
 
 
-@pytest.mark.parametrize("M,K,N,r", [(20, 192, 100, 4), (70, 512, 257, 12)])
+@pytest.mark.parametrize("M,K,N,r", [(20, 192, 100, 4), (70, 512, 257, 12), (130, 512, 256, 16), (300, 768, 192, 72)])
 def test_backward_packed_matches_oracle(M, K, N, r):
     c = _case(M, K, N, r, 5)
     dx, dA, dB = q.qerl_nvfp4_lora_linear_bwd_packed(c.dy, c.x, c.packed, c.scales, c.ts, c.A, c.B, c.s)
