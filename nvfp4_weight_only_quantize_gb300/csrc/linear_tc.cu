@@ -54,7 +54,7 @@ constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
 constexpr int RAW_CODES = TILE_N * GK * BK / 2;    // 16 KB: 128 rows x 128 code bytes (SW128)
 constexpr int RAW_SCALES = TILE_N * GK * BK / 16;  // 2 KB: 128 rows x 16 scale bytes
 constexpr int RAW_STAGE = RAW_CODES + RAW_SCALES;  // 18 KB, a multiple of 1024
-constexpr int MAX_SPLITS = 8;  // split-K factor cap: bounds the fixup's partial reads
+constexpr int MAX_SPLITS = 8;  // split-K factor cap: bounds the partial traffic
 
 template <int BN>
 struct Cfg {
@@ -102,7 +102,6 @@ struct TcFwdParams {
     const float *tensor_scale;
     __nv_bfloat16 *y;
     float *partial;
-    uint32_t *counters;
     unsigned int *err;
     unsigned long long timeout_ns;
     int fault;           // test hook: CTA 0 withholds one arrival so its waits time out
@@ -197,8 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *acc_full = stage_empty + C::S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *last_flag = abort_flag + 1;
-    volatile int *ep_ok = last_flag + 1;  // [4]: epilogue warps' view of acc_full
+    volatile int *ep_ok = abort_flag + 1;  // [4]: epilogue warps' view of acc_full
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // blockIdx.x = (split * m_tiles + m_tile) * n_tiles + n_tile; n_tiles % cs == 0, so
@@ -249,7 +247,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(acc_full, 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == WARP_RAW && lane == 0) {
@@ -519,6 +516,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 } else {
+                    // this split's FP32 partial tile [token][row]; the chained
+                    // split-K reduction kernel sums the splits
                     float *part = p.partial + ((size_t)tile * p.splits + split) * (size_t)(TILE_N * BN);
                     for (int c0 = 0; c0 < BN; c0 += 16) {
                         float v[16];
@@ -526,64 +525,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * TILE_N + row, v[j]);
                     }
-                    __threadfence();
-                    named_bar_sync(1, 128);
-                    if (threadIdx.x == 0) {
-                        const unsigned int old = atomicAdd(&p.counters[tile], 1u);
-                        *last_flag = (old == (unsigned int)(p.splits - 1)) ? 1 : 0;
-                    }
                 }
             }
         }
     }
 
-    tc_fence_before();
-    __syncthreads();
-    if (p.splits > 1 && *last_flag) {
-        // Last split of this tile: the whole CTA sums the partials in split
-        // order (deterministic), four rows per item with 16-byte loads.
-        __threadfence();
-        const float st = *p.tensor_scale;
-        const float ysc = st * pow2f(tc_exponent_offset(st));
-        const float *base = p.partial + (size_t)tile * p.splits * (size_t)(TILE_N * BN);
-        constexpr int ITEMS = BN * (TILE_N / 4);
-        for (int it0 = threadIdx.x; it0 < ITEMS; it0 += 2 * NUM_THREADS) {
-            float4 v[2][MAX_SPLITS];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int it = it0 + h * NUM_THREADS;
-                const int col = it / (TILE_N / 4), rq = (it % (TILE_N / 4)) * 4;
-#pragma unroll
-                for (int s2 = 0; s2 < MAX_SPLITS; ++s2)
-                    v[h][s2] = (it < ITEMS && s2 < p.splits)
-                                   ? __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN) +
-                                                                            (size_t)col * TILE_N + rq))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int it = it0 + h * NUM_THREADS;
-                if (it >= ITEMS) break;
-                const int col = it / (TILE_N / 4), rq = (it % (TILE_N / 4)) * 4;
-                const int m = m0 + col;
-                if (m >= p.M) continue;
-                float a4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int s2 = 0; s2 < MAX_SPLITS; ++s2) {  // fixed split order
-                    a4[0] += v[h][s2].x;
-                    a4[1] += v[h][s2].y;
-                    a4[2] += v[h][s2].z;
-                    a4[3] += v[h][s2].w;
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int n = n0 + rq + e;
-                    if (n < p.N) p.y[(size_t)m * p.N + n] = __float2bfloat16_rn(a4[e] * ysc);
-                }
-            }
-        }
-        if (threadIdx.x == 0) p.counters[tile] = 0u;
-    }
     tc_fence_before();
     __syncthreads();
     if (warp == WARP_MMA) {
@@ -601,21 +547,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // kernel reads as extra K steps, plus t_out when requested.  One CTA computes
 // MB token rows x JB adapter rows; its 256 threads stride over K in 8-element
 // vectors and the partial sums are reduced in shared memory in a fixed order.
-// CTA 0 also clears the split-K tile counters of the main kernel, which is
-// allowed to start (programmatic launch) while this kernel runs.
+// The main kernel may start (programmatic launch) while this kernel runs.
 constexpr int LD_THREADS = 256;
 
 template <int MB, int JB>
 __global__ void __launch_bounds__(LD_THREADS)
     lora_down_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ A, int M, int K, int r,
                      int r_pad, float s, const float *__restrict__ tensor_scale, float *__restrict__ t_out,
-                     __nv_bfloat16 *__restrict__ u, uint32_t *__restrict__ counters, int n_counters)
+                     __nv_bfloat16 *__restrict__ u)
 {
     __shared__ float red[LD_THREADS / 32][MB * JB];
     pdl_trigger();  // the main kernel may start streaming its weight now
-    pdl_wait();     // chained launch: x, A and the counters follow the preceding work
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
+    pdl_wait();     // chained launch: x and A follow the preceding work
     const int jgroups = r_pad / JB;
     const int m0 = (blockIdx.x / jgroups) * MB, j0 = (blockIdx.x % jgroups) * JB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -682,11 +625,57 @@ __global__ void __launch_bounds__(LD_THREADS)
     }
 }
 
+// Split-K reduction of the forward: y[m, n] = bf16(s_t 2^c * sum over splits of
+// the FP32 partial tiles), the splits summed in order (deterministic).  One
+// thread per four rows n of one token m (16-byte partial loads).  Chained
+// after the main kernel: it waits for that grid before reading.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ partial, int splits, int n_tiles,
+                                                            int m_tiles, int BN, int M, int N,
+                                                            const float *__restrict__ tensor_scale,
+                                                            __nv_bfloat16 *__restrict__ y)
+{
+    pdl_trigger();
+    pdl_wait();
+    const float st = *tensor_scale;
+    const float ysc = st * pow2f(tc_exponent_offset(st));
+    const int64_t items = (int64_t)n_tiles * m_tiles * BN * (TILE_N / 4);
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (int64_t)gridDim.x * blockDim.x) {
+        const int rq = (int)(it % (TILE_N / 4)) * 4;
+        const int64_t rest = it / (TILE_N / 4);
+        const int col = (int)(rest % BN);
+        const int64_t tile = rest / BN;  // m_tile * n_tiles + n_tile
+        const int n_tile = (int)(tile % n_tiles), m_tile = (int)(tile / n_tiles);
+        const int m = m_tile * BN + col, n = n_tile * TILE_N + rq;
+        if (m >= M || n >= N) continue;
+        const float *base = partial + (size_t)tile * splits * (size_t)(TILE_N * BN) + (size_t)col * TILE_N + rq;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < splits; ++s2) {  // fixed split order
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN)));
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        }
+        __nv_bfloat16 *dst = y + (size_t)m * N + n;
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * ysc, a.y * ysc);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * ysc, a.w * ysc);
+        if ((N & 3) == 0 && n + 4 <= N) {
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t *>(&lo);
+            w.y = *reinterpret_cast<const uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(dst) = w;
+        } else {
+            const __nv_bfloat16 v4[4] = {lo.x, lo.y, hi.x, hi.y};
+            for (int e = 0; e < 4 && n + e < N; ++e) dst[e] = v4[e];
+        }
+    }
+}
+
 // ------------------------------------------------------------------ host side
 
 struct FwdPlan {
     int BN = 0, n_tiles = 0, m_tiles = 0, splits = 1, sps = 0, nk = 0, lora_steps = 0, r_pad = 0;
-    size_t off_u = 0, off_cnt = 0, off_part = 0, total = 0;
+    size_t off_u = 0, off_part = 0, total = 0;
 };
 
 FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
@@ -712,8 +701,7 @@ FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
     pl.sps = (pl.sps + GK - 1) / GK * GK;  // splits start on a raw-stage boundary
     pl.splits = (pl.nk + pl.sps - 1) / pl.sps;  // no empty split
     pl.off_u = 0;
-    pl.off_cnt = round256(size_t(M) * pl.r_pad * 2);
-    pl.off_part = pl.off_cnt + round256(size_t(tiles) * 4);
+    pl.off_part = round256(size_t(M) * pl.r_pad * 2);
     pl.total = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
     return pl;
 }
@@ -863,7 +851,6 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     const FwdPlan pl = plan_fwd(a.M, a.N, a.K, a.r);
     if (ws_bytes < pl.total) return QERL_ERR_WORKSPACE;
     __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u);
-    uint32_t *counters = reinterpret_cast<uint32_t *>(ws + pl.off_cnt);
     float *partial = reinterpret_cast<float *>(ws + pl.off_part);
     const int tiles = pl.n_tiles * pl.m_tiles;
 
@@ -891,13 +878,13 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
             QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
                                        a.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, a.tensor_scale,
-                                       a.t_out, u, counters, tiles)));
+                                       a.t_out, u)));
         } else {
             constexpr int MB = 8, JB = 4;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
             QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
                                        a.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, a.tensor_scale,
-                                       a.t_out, u, counters, tiles)));
+                                       a.t_out, u)));
         }
     }
 
@@ -919,19 +906,26 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     p.tensor_scale = a.tensor_scale;
     p.y = a.y;
     p.partial = partial;
-    p.counters = counters;
     p.err = error_word();
     p.timeout_ns = env().timeout_ns;
     p.fault = env().fault;
     p.chain = chain ? 1 : 0;
     const unsigned grid = (unsigned)(tiles * pl.splits);
+    qerl_status st;
     switch (pl.BN) {
-    case 16: return launch_fwd<16>(cm, xm, um, sm, p, grid, a.packed != 0, s);
-    case 32: return launch_fwd<32>(cm, xm, um, sm, p, grid, a.packed != 0, s);
-    case 64: return launch_fwd<64>(cm, xm, um, sm, p, grid, a.packed != 0, s);
-    case 128: return launch_fwd<128>(cm, xm, um, sm, p, grid, a.packed != 0, s);
-    default: return launch_fwd<256>(cm, xm, um, sm, p, grid, a.packed != 0, s);
+    case 16: st = launch_fwd<16>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
+    case 32: st = launch_fwd<32>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
+    case 64: st = launch_fwd<64>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
+    case 128: st = launch_fwd<128>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
+    default: st = launch_fwd<256>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
     }
+    if (st != QERL_OK || pl.splits == 1) return st;
+    // 3) split-K: sum the partial tiles (chained: waits for the main grid)
+    const int64_t items = tiles * pl.BN * (TILE_N / 4);
+    int64_t g = (items + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    return launched(launch_k(splitk_reduce_kernel, dim3((unsigned)g), dim3(256), 0, s, chain, (const float *)partial,
+                             pl.splits, pl.n_tiles, pl.m_tiles, pl.BN, (int)a.M, (int)a.N, a.tensor_scale, a.y));
 }
 
 }  // namespace qerl
