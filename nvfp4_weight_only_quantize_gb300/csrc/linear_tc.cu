@@ -56,7 +56,13 @@ constexpr int RAW_SCALES = TILE_N * GK * BK / 16;  // 2 KB: 128 rows x 16 scale 
 constexpr int RAW_STAGE = RAW_CODES + RAW_SCALES;  // 18 KB, a multiple of 1024
 constexpr int MAX_SPLITS = 8;  // split-K factor cap: bounds the partial traffic
 
-template <int BN>
+// FUSED: the LoRA down-projection runs inside the kernel (decode tiles, r <= 32,
+// no t output): per main k-step one more MMA accumulates t_s^T = A x^T over the
+// CTA's k-range in TMEM, and the CTA builds u_s = bf16(s t_s / (s_t 2^c)) in
+// shared memory for its own LoRA step (the sum over splits of s t_s B^T is the
+// LoRA term).
+constexpr int FUSED_R = 32;  // LoRA rows loaded per k-step in fused mode
+template <int BN, bool FUSED = false>
 struct Cfg {
     // k-steps per pipeline stage: every stage costs the MMA issuer one barrier
     // round trip and one commit, so small token tiles (short MMAs) take two.
@@ -70,23 +76,28 @@ struct Cfg {
     static_assert(S >= DQ_GROUPS, "parity waits need at least one stage per dequant group");
     // Token-tile stages (smem), deeper than the A ring: a token slot is reloaded
     // only after the MMA that read it completed, a ~2 us round trip.
-    static constexpr int XS = BN >= 128 ? 2 : 4;
-    static constexpr int LOG_XS = BN >= 128 ? 1 : 2;
+    static constexpr int XS = FUSED ? 3 : (BN >= 128 ? 2 : 4);
     static constexpr int R = 4;  // raw (code+scale) stages
     static_assert(GK % SPS == 0 && GK / SPS <= DQ_GROUPS, "each group has at most one stage per raw stage");
-    static_assert((1 << LOG_XS) == XS, "power-of-two token ring");
     static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
     static_assert(R * GK >= S * SPS, "raw ring deep enough for parity-safe waits");
     static constexpr int X_STEP = BN * BK * 2;
     static constexpr int X_STAGE = X_STEP * SPS;
+    // fused: the LoRA A rows of each k-step (FUSED_R x 64 bf16, 128-byte rows)
+    static constexpr int AL_STEP = FUSED_R * BK * 2;
+    static constexpr int AL_STAGE = FUSED ? AL_STEP * SPS : 0;
     // TMEM: the f32 accumulator (BN columns), then S A stages of 32*SPS columns
     // (128 rows x 64 bf16 per step, two per 32-bit column).
     static constexpr int A_COL0 = BN < 32 ? 32 : BN;
-    static constexpr int TMEM_NEED = A_COL0 + S * 32 * SPS;
+    static constexpr int T_COL = A_COL0 + S * 32 * SPS;  // fused: t_s^T accumulator
+    static constexpr int TMEM_NEED = T_COL + (FUSED ? (BN < 32 ? 32 : BN) : 0);
     static constexpr int TMEM_COLS = TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512));
     static_assert(TMEM_NEED <= 512, "TMEM holds 512 columns");
     static constexpr int BAR_BYTES = 1024;
-    static constexpr int SMEM = XS * X_STAGE + R * RAW_STAGE + BAR_BYTES + 1024;
+    // token ring, fused LoRA-A ring (an MMA reads 128 rows = 16 KB from each
+    // step's start, so the raw ring must follow it), raw ring, barriers
+    static constexpr int SMEM = XS * X_STAGE + XS * AL_STAGE + R * RAW_STAGE + BAR_BYTES + 1024;
+    static_assert(!FUSED || R * RAW_STAGE >= 16384, "the LoRA-A MMA window stays inside shared memory");
     static_assert(XS * X_STAGE >= BN * TILE_N * 2, "the y staging tile reuses the token ring");
 };
 
@@ -106,6 +117,7 @@ struct TcFwdParams {
     unsigned long long timeout_ns;
     int fault;           // test hook: CTA 0 withholds one arrival so its waits time out
     int chain;           // launched chained: token tiles and B wait for the preceding grid
+    float lora_scale;    // fused: s
     int cs;              // CTAs per cluster (1, 2 or 4): consecutive weight tiles sharing one
                          // token tile per stage, each CTA loading 1/cs of it for all (multicast)
 };
@@ -174,18 +186,19 @@ __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-template <int BN, bool PACKED>
+template <int BN, bool PACKED, bool FUSED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap x_map,
                   const __grid_constant__ CUtensorMap u_map, const __grid_constant__ CUtensorMap scl_map,
-                  const TcFwdParams p)
+                  const __grid_constant__ CUtensorMap al_map, const TcFwdParams p)
 {
-    using C = Cfg<BN>;
+    using C = Cfg<BN, FUSED>;
     constexpr int SPS = C::SPS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *X_ring = smem;
-    uint8_t *R_ring = X_ring + C::XS * C::X_STAGE;
+    uint8_t *AL_ring = X_ring + C::XS * C::X_STAGE;  // fused: LoRA A rows per k-step
+    uint8_t *R_ring = AL_ring + C::XS * C::AL_STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(R_ring + C::R * RAW_STAGE);
     uint64_t *raw_full = bars;
     uint64_t *raw_empty = raw_full + C::R;
@@ -194,7 +207,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *a_full = x_empty + C::XS;
     uint64_t *stage_empty = a_full + C::S;  // MMA of the stage done: frees its A tile
     uint64_t *acc_full = stage_empty + C::S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *t_full = acc_full + 1;  // fused: every t_s MMA done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(t_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *ep_ok = abort_flag + 1;  // [4]: epilogue warps' view of acc_full
 
@@ -214,7 +228,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int k_end = min(p.nk, k_begin + p.steps_per_split);
     const int n_main = k_end > k_begin ? k_end - k_begin : 0;  // a multiple of GK (K % 256 == 0)
     const int n_groups = n_main / GK;
-    const int n_steps = n_main + (split == p.splits - 1 ? p.lora_steps : 0);
+    // The LoRA steps belong to the last split, or (fused) to every split.
+    const int n_steps = n_main + ((FUSED || split == p.splits - 1) ? p.lora_steps : 0);
     const int n_stages = (n_steps + SPS - 1) / SPS;  // the last (LoRA) stage may be partial
     const int main_stages = n_main / SPS;
     // Every CTA walks its k-range from a different raw group, so that the CTAs
@@ -246,6 +261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&stage_empty[i], 1);
         }
         mbar_init(acc_full, 1);
+        mbar_init(t_full, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -255,7 +271,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (warp == WARP_X && lane == 0) {
         prefetch_tensormap(&x_map);
-        prefetch_tensormap(&u_map);
+        if (FUSED)
+            prefetch_tensormap(&al_map);
+        else
+            prefetch_tensormap(&u_map);
     }
     if (warp == WARP_MMA) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -316,6 +335,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     drain_wait(&raw_full[g % C::R], (uint32_t)(g / C::R) & 1u);
         }
         __syncwarp();
+        if (FUSED && n_stages > main_stages) {
+            // ------------------------------------------- u_s for this CTA's LoRA step
+            // Lane j reads row j of t_s^T (TMEM lanes 0-31 belong to this warp)
+            // and writes column j of the step's token tile: u_s[m][j] =
+            // bf16(s t_s[m][j] / (s_t 2^c)), columns 32..63 zero.
+            const int slot = main_stages % C::XS;
+            const uint32_t round = (uint32_t)(main_stages / C::XS);
+            bool ok = __all_sync(0xFFFFFFFFu, wait(t_full, 0));
+            if (ok && round > 0) ok = __all_sync(0xFFFFFFFFu, wait(&x_empty[slot], (round - 1) & 1u));
+            if (ok) {
+                tc_fence_after();
+                const float st = *p.tensor_scale;
+                const float fac = p.lora_scale / (st * pow2f(tc_exponent_offset(st)));
+                const uint32_t sdst = smem_u32(X_ring + slot * C::X_STAGE);
+                const bool jv = lane < p.r;
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    uint32_t tr[16];
+                    tmem_ld16(tmem + (uint32_t)C::T_COL + (uint32_t)c0, tr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int m = c0 + e;
+                        const __nv_bfloat16 uv = __float2bfloat16_rn(jv ? __uint_as_float(tr[e]) * fac : 0.0f);
+                        const uint32_t rowb = sdst + (uint32_t)(m * 128);
+                        const uint32_t lo = (uint32_t)((((lane >> 3) ^ (m & 7)) << 4) | ((lane & 7) << 1));
+                        const uint32_t hi = (uint32_t)(((((lane + 32) >> 3) ^ (m & 7)) << 4) | ((lane & 7) << 1));
+                        asm volatile("st.shared.b16 [%0], %1;" ::"r"(rowb + lo), "h"(*reinterpret_cast<const unsigned short *>(&uv))
+                                     : "memory");
+                        asm volatile("st.shared.b16 [%0], %1;" ::"r"(rowb + hi), "h"((unsigned short)0) : "memory");
+                    }
+                }
+                fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&x_full[slot]);
+            }
+        }
     } else if (warp == WARP_X) {
         // ------------------------------------------- token tiles (SPS per stage)
         if (lane == 0) {
@@ -325,17 +380,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // grid, which that grid waited for; wait for it before any x tile.
             if (p.chain) pdl_wait();
             for (int j = 0; j < n_stages; ++j) {
-                const int slot = j & (C::XS - 1);
-                const uint32_t round = (uint32_t)(j >> C::LOG_XS);
+                const int slot = j % C::XS;
+                const uint32_t round = (uint32_t)(j / C::XS);
                 // u is written by the LoRA down-projection launched just before
                 // this kernel, which lets this grid start early (programmatic
                 // launch): wait for that grid only before the first u tile.  The
                 // token tiles x were complete before that grid was launched.
+                if (FUSED && j >= main_stages) break;  // u is built in this CTA
                 if (j == main_stages) asm volatile("griddepcontrol.wait;" ::: "memory");
                 if (round > 0 && !wait(&x_empty[slot], (round - 1) & 1u)) break;
                 const int nsub = min(SPS, n_steps - j * SPS);
-                mbar_arrive_expect_tx(&x_full[slot], (uint32_t)(C::X_STEP * nsub));
+                mbar_arrive_expect_tx(&x_full[slot], (uint32_t)((C::X_STEP + (FUSED ? C::AL_STEP : 0)) * nsub));
                 uint8_t *dst = X_ring + slot * C::X_STAGE;
+                if (FUSED) {  // LoRA A rows 0..31 (zero past r) of each k-step
+#pragma unroll
+                    for (int sub = 0; sub < SPS; ++sub) {
+                        if (sub >= nsub) break;
+                        tma_load_2d_hint(AL_ring + slot * C::AL_STAGE + sub * C::AL_STEP, &al_map, &x_full[slot],
+                                         kstep(j * SPS + sub) * BK, 0, pol);
+                    }
+                }
 #pragma unroll
                 for (int sub = 0; sub < SPS; ++sub) {
                     if (sub >= nsub) break;
@@ -351,7 +415,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (*abort_flag)
                 for (int j = issued > C::XS ? issued - C::XS : 0; j < issued; ++j)
-                    drain_wait(&x_full[j & (C::XS - 1)], (uint32_t)(j >> C::LOG_XS) & 1u);
+                    drain_wait(&x_full[j % C::XS], (uint32_t)(j / C::XS) & 1u);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
@@ -363,7 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t at0 = tmem + (uint32_t)C::A_COL0;
         bool ready = n_stages > 0 && __all_sync(0xFFFFFFFFu, wait(&a_full[0], 0) && wait(&x_full[0], 0));
         for (int j = 0; j < n_stages && ready; ++j) {
-            const int s = j % C::S, xs = j & (C::XS - 1);
+            const int s = j % C::S, xs = j % C::XS;
             const int nsub = min(SPS, n_steps - j * SPS);
             tc_fence_after();
             if (elect_one()) {
@@ -377,7 +441,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         umma_bf16_ts(tmem, at + (uint32_t)(sub * 32 + 8 * kk),
                                      bd + (uint64_t)((sub * C::X_STEP) >> 4) + 2u * kk, idesc,
                                      (j > 0 || sub > 0 || kk > 0) ? 1u : 0u);
+                    if (FUSED && j < main_stages) {
+                        // t_s^T += A[0..127 (rows >= 32 unused), k-step] x^T: the same token
+                        // tile as B; the LoRA A rows from shared memory as A
+                        const uint64_t ad = desc_kmajor_sw128(smem_u32(AL_ring + xs * C::AL_STAGE + sub * C::AL_STEP));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16(tmem + (uint32_t)C::T_COL, ad + 2u * kk,
+                                      bd + (uint64_t)((sub * C::X_STEP) >> 4) + 2u * kk, idesc,
+                                      (j > 0 || sub > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
+                if (FUSED && j == main_stages - 1) umma_commit(t_full);
                 umma_commit(&stage_empty[s]);
                 if (cs == 1)
                     umma_commit(&x_empty[xs]);
@@ -386,9 +461,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             __syncwarp();
             if (j + 1 < n_stages) {
-                const int s1 = (j + 1) % C::S, xs1 = (j + 1) & (C::XS - 1);
+                const int s1 = (j + 1) % C::S, xs1 = (j + 1) % C::XS;
                 ready = __all_sync(0xFFFFFFFFu, wait(&a_full[s1], (uint32_t)((j + 1) / C::S) & 1u) &&
-                                                    wait(&x_full[xs1], (uint32_t)((j + 1) >> C::LOG_XS) & 1u));
+                                                    wait(&x_full[xs1], (uint32_t)((j + 1) / C::XS) & 1u));
             }
         }
         // Arrives once every MMA issued above has completed (also after an abort).
@@ -717,8 +792,11 @@ struct Env {
     unsigned long long timeout_ns = 2000000000ull;  // 2 s
     int fault = 0;
     int cluster = 0;  // QERL_TC_CLUSTER = 1, 2 or 4 forces that cluster size (tests)
+    int no_fuse = 0;  // QERL_TC_NO_FUSE = 1: separate down-projection grid always (tests)
     Env()
     {
+        const char *nf = std::getenv("QERL_TC_NO_FUSE");
+        if (nf && nf[0] == '1') no_fuse = 1;
         const char *c = std::getenv("QERL_TC_CLUSTER");
         if (c && (c[0] == '1' || c[0] == '2' || c[0] == '4') && c[1] == 0) cluster = c[0] - '0';
         const char *f = std::getenv("QERL_TEST_WITHHOLD_ARRIVAL");
@@ -776,36 +854,38 @@ int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int n_tiles, unsigned gr
     return 1;
 }
 
-template <int BN>
+template <int BN, bool FUSED>
 qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const CUtensorMap &sm,
-                       const TcFwdParams &p0, unsigned grid, bool packed, cudaStream_t s)
+                       const CUtensorMap &alm, const TcFwdParams &p0, unsigned grid, bool packed, bool pdl,
+                       cudaStream_t s)
 {
-    auto kernel = packed ? tc_fwd_kernel<BN, true> : tc_fwd_kernel<BN, false>;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM) != cudaSuccess)
+    using C = Cfg<BN, FUSED>;
+    auto kernel = packed ? tc_fwd_kernel<BN, true, FUSED> : tc_fwd_kernel<BN, false, FUSED>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return QERL_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     TcFwdParams p = p0;
     // Decode-sized token tiles are cheap to load per CTA, and clusters would tie
     // the CTAs' pipelines together; wide (prefill) tiles share them.
     p.cs = pick_cluster<(BN >= 256)>(kernel, cfg, p.n_tiles, grid);
-    // Programmatic dependent launch: the CTAs may start while the LoRA
-    // down-projection still runs and stream their (static) weights; the token
-    // producer waits for it with griddepcontrol.wait.  Clusters of p.cs CTAs
-    // share the token tiles (multicast).
+    // Programmatic dependent launch: the CTAs may start while the preceding
+    // grid still runs and stream their (frozen) weights; the token producer and
+    // the epilogue wait for that grid with griddepcontrol.wait.  Clusters of
+    // p.cs CTAs share the token tiles (multicast).
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = (unsigned)p.cs;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kernel, cm, xm, um, sm, p) != cudaSuccess) return QERL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, cm, xm, um, sm, alm, p) != cudaSuccess) return QERL_ERR_CUDA;
     return launched();
 }
 
@@ -854,9 +934,14 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     float *partial = reinterpret_cast<float *>(ws + pl.off_part);
     const int tiles = pl.n_tiles * pl.m_tiles;
 
-    CUtensorMap cm, xm, um, sm;
+    // Fused LoRA down-projection (no separate grid) for decode tiles split over
+    // K when t is not requested.  Unsplit linears keep the separate grid: it
+    // overlaps their long weight stream, while the fused MMAs would load it.
+    const bool fused = !a.t_out && pl.BN <= 64 && a.r <= FUSED_R && pl.splits > 1 && !env().no_fuse;
+    CUtensorMap cm, xm, um, sm, alm;
     // codes: 128 rows x 128 bytes (4 k-steps) per box, 128-byte swizzle; scales:
-    // 128 rows x 16 bytes (the same 4 k-steps); token tiles: BN rows x 64 bf16.
+    // 128 rows x 16 bytes (the same 4 k-steps); token tiles: BN rows x 64 bf16;
+    // fused: LoRA A rows 0..31 x 64 bf16 (zero past r).
     if (!make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, a.K / 2, a.N, a.K / 2, GK * BK / 2, TILE_N,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&sm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, a.K / 16, a.N, a.K / 16, GK * BK / 16, TILE_N,
@@ -864,6 +949,8 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
         !make_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, a.K * 2, BK, pl.BN,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&um, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, pl.r_pad, a.M, pl.r_pad * 2, BK, pl.BN,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&alm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, a.K, a.r, a.K * 2, BK, FUSED_R,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return QERL_ERR_CUDA;
 
@@ -872,7 +959,7 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     //    and the main kernel may then stream and dequantize its (frozen) weight
     //    while that work is still running.
     const bool chain = g_chain.load() != 0;
-    {
+    if (!fused) {
         if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
             constexpr int MB = 4, JB = 2;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
@@ -910,14 +997,27 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     p.timeout_ns = env().timeout_ns;
     p.fault = env().fault;
     p.chain = chain ? 1 : 0;
+    p.lora_scale = a.lora_scale;
     const unsigned grid = (unsigned)(tiles * pl.splits);
     qerl_status st;
+    // The main kernel follows the down-projection grid programmatically; fused,
+    // it follows the preceding work when launches are chained.
+    const bool pk = a.packed != 0, pdl = fused ? chain : true;
     switch (pl.BN) {
-    case 16: st = launch_fwd<16>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
-    case 32: st = launch_fwd<32>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
-    case 64: st = launch_fwd<64>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
-    case 128: st = launch_fwd<128>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
-    default: st = launch_fwd<256>(cm, xm, um, sm, p, grid, a.packed != 0, s); break;
+    case 16:
+        st = fused ? launch_fwd<16, true>(cm, xm, um, sm, alm, p, grid, pk, pdl, s)
+                   : launch_fwd<16, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s);
+        break;
+    case 32:
+        st = fused ? launch_fwd<32, true>(cm, xm, um, sm, alm, p, grid, pk, pdl, s)
+                   : launch_fwd<32, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s);
+        break;
+    case 64:
+        st = fused ? launch_fwd<64, true>(cm, xm, um, sm, alm, p, grid, pk, pdl, s)
+                   : launch_fwd<64, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s);
+        break;
+    case 128: st = launch_fwd<128, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s); break;
+    default: st = launch_fwd<256, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s); break;
     }
     if (st != QERL_OK || pl.splits == 1) return st;
     // 3) split-K: sum the partial tiles (chained: waits for the main grid)

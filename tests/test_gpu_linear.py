@@ -137,3 +137,11 @@ def test_qwen7b_backward_full_size(lin):
     rng = np.random.default_rng(lin)
     _bwd_check(c, dx_rows=np.array([0, 8191]), dA_cols=np.sort(rng.choice(K, 8, replace=False)),
                dB_rows=np.sort(rng.choice(N, 8, replace=False)))
+
+
+@pytest.mark.parametrize("M,K,N,r", [(1, 256, 128, 1), (8, 512, 1024, 8), (64, 3584, 3584, 32), (37, 1024, 384, 16),
+                                     (64, 18944, 512, 32), (16, 2048, 18944, 32), (33, 768, 200, 5)])
+def test_forward_without_t(M, K, N, r):
+    """Decode shapes with no t output take the fused down-projection path."""
+    c = LinearCase(M, K, N, r, config=9, idx=M * 7 + r).quantize_gpu()
+    _fwd_check(c, rows=None if M * N <= 200_000 else np.arange(min(M, 4)), want_t=False)

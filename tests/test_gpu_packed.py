@@ -76,17 +76,25 @@ def test_forward_packed_matches_oracle_and_standard(algo, M, K, N, r):
     try:
         c = _case(M, K, N, r, M + N)
         t = torch.empty(M, r, dtype=torch.float32, device="cuda")
+        t2 = torch.empty(M, r, dtype=torch.float32, device="cuda")
         yp = q.qerl_nvfp4_lora_linear_fwd_packed(c.x, c.packed, c.scales, c.ts, c.A, c.B, c.s, t_out=t)
-        ys = q.qerl_nvfp4_lora_linear_fwd(c.x, c.codes, c.scales, c.ts, c.A, c.B, c.s)
+        ys = q.qerl_nvfp4_lora_linear_fwd(c.x, c.codes, c.scales, c.ts, c.A, c.B, c.s, t_out=t2)
+        # without t (decode tiles take the fused down-projection)
+        yp0 = q.qerl_nvfp4_lora_linear_fwd_packed(c.x, c.packed, c.scales, c.ts, c.A, c.B, c.s)
+        ys0 = q.qerl_nvfp4_lora_linear_fwd(c.x, c.codes, c.scales, c.ts, c.A, c.B, c.s)
         torch.cuda.synchronize()
         assert q.get_error() == 0
     finally:
         q.set_linear_algo(q.ALGO_AUTO)
-    assert torch.equal(yp, ys)  # same arithmetic, only the code layout differs
+    # same arithmetic, only the code layout differs
+    assert torch.equal(yp, ys)
+    assert torch.equal(yp0, ys0)
+    assert torch.equal(t, t2)
     oc, osc, ost = c.oracle_quant()
     ref, tref = oracle.lora_linear_fwd(synth.bits(c.x), oc, osc, ost, synth.bits(c.A), synth.bits(c.B), c.s,
                                        want_t=True)
     assert_rel_rms(f64(yp), ref, LIN_TOL, "y")
+    assert_rel_rms(f64(yp0), ref, LIN_TOL, "y without t")
     assert_rel_rms(f64(t), tref, 1e-5, "t")
 
 
