@@ -358,7 +358,7 @@ def _time_fn(fn, reps, warm=3):
     return e0.elapsed_time(e1) / 1e3 / reps
 
 
-def other_rows(dev):
+def other_rows(dev, only=None, profile=False):
     """Each remaining hot-path row on its own workload (CUDA events, after warm-up):
     the quantizer on a Qwen2.5-7B gate_proj weight, AQN-RMSNorm at decode and
     prefill sizes, the Qwen2.5-14B prefill linears (M = 4096) and one Qwen2.5-7B
@@ -366,31 +366,47 @@ def other_rows(dev):
     import nvfp4_weight_only_quantize_gb300 as q
     from nvfp4_weight_only_quantize_gb300 import synth
     rows = {}
+    want = (lambda row: only is None or only == row)
+
+    def timed(fn, reps, warm=3):
+        # with --profile-row, ncu (--profile-from-start off) sees only the timed launches
+        if profile:
+            fn()
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaProfilerStart()
+        sec = _time_fn(fn, reps, warm=0 if profile else warm)
+        if profile:
+            torch.cuda.cudart().cudaProfilerStop()
+        return sec
     # a1: 18944 x 3584 bf16 (136 MB, above L2); algorithmic bytes = read W once + write codes/scales
     N, K = 18944, 3584
-    W = synth.weight(N, K, 11, dev)
+    W = synth.weight(N, K, 11, dev) if want("a1") else None
     codes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
     scales = torch.empty(N, K // 16, dtype=torch.uint8, device=dev)
     ts = torch.empty(1, dtype=torch.float32, device=dev)
     wsq = q.workspace(q.OP_QUANTIZE, 0, N, K, 0, dev)
-    sec = _time_fn(lambda: q.qerl_nvfp4_quantize(W, out=(codes, scales, ts), ws=wsq), 20)
-    rows["a1_quantize"] = {"workload": f"qwen2.5-7b gate_proj weight {N}x{K} bf16", "us": round(sec * 1e6, 1),
+    sec = timed(lambda: q.qerl_nvfp4_quantize(W, out=(codes, scales, ts), ws=wsq), 20) if want("a1") else 0.0
+    if want("a1"):
+        rows["a1_quantize"] = {"workload": f"qwen2.5-7b gate_proj weight {N}x{K} bf16", "us": round(sec * 1e6, 1),
                            "GBps": round(N * K * 2.5625 / sec / 1e9, 1),
-                           "bytes": "2 B read + 0.5625 B written per weight (the kernel reads W twice)"}
+                               "bytes": "2 B read + 0.5625 B written per weight (the kernel reads W twice)"}
     del W
     # a2: decode and prefill norms
-    for M, H, tag in [(64, 3584, "decode M=64 H=3584"), (4096, 5120, "prefill M=4096 H=5120")]:
+    for M, H, tag in ([(64, 3584, "decode M=64 H=3584"), (4096, 5120, "prefill M=4096 H=5120")] if want("a2") else []):
         x = synth.activations(M, H, 12, dev)
         g = synth.norm_gamma(H, 13, dev)
         y = torch.empty_like(x)
         wsn = q.workspace(q.OP_AQN_RMSNORM, M, 0, H, 0, dev)
-        sec = _time_fn(lambda: q.qerl_aqn_rmsnorm(x, g, 1e-6, 1e-2, 1, 5, 0, y=y, ws=wsn), 50)
+        sec = timed(lambda: q.qerl_aqn_rmsnorm(x, g, 1e-6, 1e-2, 1, 5, 0, y=y, ws=wsn), 50)
         rows[f"a2_aqn_rmsnorm_{'decode' if M == 64 else 'prefill'}"] = {
             "workload": tag, "us": round(sec * 1e6, 2), "GBps": round((4 * M * H + 6 * H) / sec / 1e9, 1)}
     # a4: Qwen2.5-14B prefill linears, M = 4096, r = 32
     wl = synth.WORKLOADS[2]
     M, tot_f, tot_s, per = 4096, 0.0, 0.0, {}
-    x = synth.activations(M, max(K for _, _, K in wl.linears), 14, dev)
+    _, bf16, _, kind = peaks()
+    if not want("a4"):
+        wl = synth.Workload(wl.name, [], wl.M, wl.r, wl.hidden)
+    x = synth.activations(M, max(K for _, _, K in wl.linears), 14, dev) if wl.linears else None
     for i, (name, N, K) in enumerate(wl.linears):
         W = synth.weight(N, K, 20 + i, dev)
         c, sc, t = q.qerl_nvfp4_quantize(W)
@@ -401,14 +417,17 @@ def other_rows(dev):
         xi = x[:, :K].contiguous()
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         ws = q.workspace(q.OP_LINEAR_FWD, M, N, K, wl.r, dev)
-        sec = _time_fn(lambda: q.qerl_nvfp4_lora_linear_fwd_packed(xi, c, sc, t, A, B, 2.0, y=y, ws=ws), 10)
+        sec = timed(lambda: q.qerl_nvfp4_lora_linear_fwd_packed(xi, c, sc, t, A, B, 2.0, y=y, ws=ws), 10)
         fl = 2.0 * M * N * K + 2.0 * M * wl.r * (N + K)
         per[name] = {"us": round(sec * 1e6, 1), "TFLOPs": round(fl / sec / 1e12, 1)}
         tot_f, tot_s = tot_f + fl, tot_s + sec
-    _, bf16, _, kind = peaks()
-    rows["a4_prefill"] = {"workload": wl.name, "TFLOPs": round(tot_f / tot_s / 1e12, 1),
-                          "frac_of_bf16_peak": round(tot_f / tot_s / 1e12 / bf16, 3),
-                          "peak": f"{kind} bf16_tflops {bf16}", "per_linear": per}
+    if want("a4"):
+        rows["a4_prefill"] = {"workload": wl.name, "TFLOPs": round(tot_f / tot_s / 1e12, 1),
+                              "frac_of_bf16_peak": round(tot_f / tot_s / 1e12 / bf16, 3),
+                              "peak": f"{kind} bf16_tflops {bf16}", "per_linear": per}
+    if not want("a5"):
+        torch.cuda.synchronize()
+        return rows
     # a5: Qwen2.5-7B q_proj backward, M = 8192, r = 32 (dx, dA, dB)
     wl = synth.WORKLOADS[4]
     name, N, K = wl.linears[0]
@@ -424,8 +443,8 @@ def other_rows(dev):
     dA = torch.empty(wl.r, K, dtype=torch.float32, device=dev)
     dB = torch.empty(N, wl.r, dtype=torch.float32, device=dev)
     ws = q.workspace(q.OP_LINEAR_BWD, M, N, K, wl.r, dev)
-    sec = _time_fn(lambda: q.qerl_nvfp4_lora_linear_bwd(dy, x, c, sc, t, A, B, 2.0, dx=dx, dA=dA, dB=dB, ws=ws), 3,
-                   warm=1)
+    sec = timed(lambda: q.qerl_nvfp4_lora_linear_bwd(dy, x, c, sc, t, A, B, 2.0, dx=dx, dA=dA, dB=dB, ws=ws), 3,
+                warm=1)
     fl = 2.0 * M * N * K + 2.0 * M * wl.r * (3 * N + 2 * K)
     rows["a5_backward"] = {"workload": f"qwen2.5-7b {name} {N}x{K}, M={M}, r={wl.r}", "us": round(sec * 1e6, 1),
                            "TFLOPs": round(fl / sec / 1e12, 2),
@@ -509,6 +528,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize/norm/prefill/backward lines")
+    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5"],
+                    help="run only that row's measurement, its timed launches bracketed by "
+                         "cudaProfilerStart/Stop (for ncu --profile-from-start off), and print it")
     ap.add_argument("--codes", default="packed", choices=["packed", "standard"],
                     help="code layout of the frozen weights (packed once at load time, or as quantized)")
     ap.add_argument("--profile-region", action="store_true",
@@ -518,6 +540,10 @@ def main():
     rank, world, local_rank = dist_init()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.profile_row:
+        torch.cuda.set_device(local_rank)
+        print(json.dumps(other_rows(torch.device("cuda", local_rank), only=args.profile_row, profile=True)),
+              flush=True)
     else:
         import nvfp4_weight_only_quantize_gb300 as q
         q.lib()  # the CUDA library must be built; no fallback

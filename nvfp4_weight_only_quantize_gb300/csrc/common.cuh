@@ -110,4 +110,18 @@ __device__ __forceinline__ float e2m1_to_float(uint32_t c)
     return (c & 8u) ? -v : v;
 }
 
+// Exponent offset c in [7, 116] with s_t * 2^c in [1, 2) when possible: the
+// tensor-core paths carry e2m1 * e4m3 * 2^-c in bf16 (then a normal bf16 range,
+// [2^-10-c, 2688 * 2^-c]) and scale by s_t * 2^c once, in FP32.
+__device__ __forceinline__ int tc_exponent_offset(float s_t)
+{
+    int e = 0;
+    frexpf(s_t, &e);
+    const int c = 1 - e;
+    return c < 7 ? 7 : (c > 116 ? 116 : c);
+}
+
+// 2^e as a float for e in the normal range (exact, unlike exp2f).
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
 }  // namespace qerl

@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(256) thin_rows_kernel(const __nv_bfloat16 *__r
 {
     constexpr int THIN_TR = thin_tr<R_PAD>(), r_pad = R_PAD;
     __shared__ __align__(16) __nv_bfloat16 Xs[THIN_TR][THIN_TK + 8];
+    pdl_trigger();
+    pdl_wait();  // chained launch: X and W follow the preceding work
     __shared__ __align__(16) float Ws[THIN_TK][68];
     const int tid = threadIdx.x;
     const int jg = tid % (r_pad / 8), rg = tid / (r_pad / 8);  // rank group (8), row group (4)
@@ -543,6 +545,30 @@ size_t thin_wide_ws(int64_t M, int64_t Wd, int r)
     return round256(size_t(thin_splits((Wd + tr - 1) / tr, M)) * Wd * r * sizeof(float));
 }
 
+// t = sum of the split partials (fixed order); t_out = t (optional); u =
+// bf16(s t / (s_t 2^c)) as [M, r_pad], zeros past r: the LoRA operand of the
+// tensor-core forward.
+__global__ void __launch_bounds__(256) u_reduce_kernel(const float *__restrict__ part, int splits, int64_t M, int r,
+                                                       int r_pad, float s, const float *__restrict__ tensor_scale,
+                                                       float *__restrict__ t_out, __nv_bfloat16 *__restrict__ u)
+{
+    pdl_trigger();
+    pdl_wait();
+    const float st = *tensor_scale;
+    const float fac = s / (st * pow2f(tc_exponent_offset(st)));
+    const int64_t n = M * r_pad;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / r_pad;
+        const int j = (int)(i % r_pad);
+        float t = 0.0f;
+        if (j < r) {
+            for (int z = 0; z < splits; ++z) t += part[(z * M + m) * r + j];
+            if (t_out) t_out[m * r + j] = t;
+        }
+        u[i] = __float2bfloat16_rn(t * fac);
+    }
+}
+
 // Scratch of the backward: v, t (when not saved), v' for the tensor-core dx,
 // and the split-k partials of the thin products.
 struct BwdWs {
@@ -630,6 +656,31 @@ qerl_status check_common(int64_t M, int64_t K, int64_t N, const uint8_t *codes, 
 }
 
 }  // namespace
+
+bool lora_down_rows_applies(int64_t K, int r) { return thin_ok(K, r); }
+size_t lora_down_rows_ws(int64_t M, int64_t K, int r) { return thin_rows_ws(M, K, r); }
+
+qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const __nv_bfloat16 *A, int r, int r_pad,
+                           float s, const float *tensor_scale, float *t_out, __nv_bfloat16 *u, float *part,
+                           bool chain, cudaStream_t st)
+{
+    const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
+    const int64_t tiles = (M + tr - 1) / tr;
+    const int sp = thin_splits(tiles, K);
+    const int64_t kchunk = ((K + sp - 1) / sp + THIN_TK - 1) / THIN_TK * THIN_TK;
+    const int splits = (int)((K + kchunk - 1) / kchunk);
+    const dim3 grid((unsigned)tiles, (unsigned)splits);
+    if (r <= 32)
+        QERL_TRY(launched(launch_k(thin_rows_kernel<true, 32>, grid, dim3(256), 0, st, chain, x, M, K, A, r, kchunk,
+                                   part)));
+    else
+        QERL_TRY(launched(launch_k(thin_rows_kernel<true, 64>, grid, dim3(256), 0, st, chain, x, M, K, A, r, kchunk,
+                                   part)));
+    int64_t g = (M * r_pad + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    return launched(launch_k(u_reduce_kernel, dim3((unsigned)g), dim3(256), 0, st, chain, (const float *)part, splits,
+                             M, r, r_pad, s, tensor_scale, t_out, u));
+}
 
 size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {

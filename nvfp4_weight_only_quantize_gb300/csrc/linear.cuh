@@ -51,6 +51,15 @@ inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
+// LoRA down-projection for many tokens (CUDA cores, split over K): t = x A^T,
+// t_out = t when given, u = bf16(s t / (s_t 2^c)) [M, r_pad] (zeros past r);
+// part holds lora_down_rows_ws(M, K, r) bytes.  Chained launches when `chain`.
+bool lora_down_rows_applies(int64_t K, int r);
+size_t lora_down_rows_ws(int64_t M, int64_t K, int r);
+qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const __nv_bfloat16 *A, int r, int r_pad,
+                           float s, const float *tensor_scale, float *t_out, __nv_bfloat16 *u, float *part,
+                           bool chain, cudaStream_t st);
+
 // Tensor-core input gradient dx = dy w_hat + s v A for the shapes it covers
 // (K % 256 == 0, N % 64 == 0, r <= 256); v = dy B in FP32 [M, r] is given, and
 // vp_ws holds tc_dx_ws_bytes(M, r) bytes of scratch.

@@ -122,19 +122,6 @@ struct TcFwdParams {
                          // token tile per stage, each CTA loading 1/cs of it for all (multicast)
 };
 
-// Exponent offset c in [7, 116] with s_t * 2^c in [1, 2) when possible: the
-// dequantized e2m1*e4m3*2^-c then lies in [2^-10-c, 2688*2^-c], a normal bf16
-// range, and the scale factor e4m3 * 2^(126-c) stays finite.
-__device__ __forceinline__ int tc_exponent_offset(float s_t)
-{
-    int e = 0;
-    frexpf(s_t, &e);
-    int c = 1 - e;
-    return c < 7 ? 7 : (c > 116 ? 116 : c);
-}
-
-// 2^e as a float for e in the normal range (exact, unlike exp2f).
-__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 // bf16x2 {f, f} with f = e4m3(b) * 2^(126 - c), exact (<= 4 significant bits).
 // b20 holds the scale byte b in bits 20..27 (other bits are masked off here).
@@ -750,7 +737,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
 
 struct FwdPlan {
     int BN = 0, n_tiles = 0, m_tiles = 0, splits = 1, sps = 0, nk = 0, lora_steps = 0, r_pad = 0;
-    size_t off_u = 0, off_part = 0, total = 0;
+    size_t off_u = 0, off_part = 0, off_rows = 0, total = 0;
 };
 
 FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
@@ -777,7 +764,9 @@ FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
     pl.splits = (pl.nk + pl.sps - 1) / pl.sps;  // no empty split
     pl.off_u = 0;
     pl.off_part = round256(size_t(M) * pl.r_pad * 2);
-    pl.total = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
+    pl.off_rows = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
+    // many tokens: the down-projection runs as a split-K rows x rank product
+    pl.total = pl.off_rows + (M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r) : 0);
     return pl;
 }
 
@@ -959,7 +948,10 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     //    and the main kernel may then stream and dequantize its (frozen) weight
     //    while that work is still running.
     const bool chain = g_chain.load() != 0;
-    if (!fused) {
+    if (!fused && a.M > 64 && lora_down_rows_applies(a.K, a.r)) {
+        QERL_TRY(lora_down_rows(a.x, a.M, a.K, a.A, a.r, pl.r_pad, a.lora_scale, a.tensor_scale, a.t_out, u,
+                                reinterpret_cast<float *>(ws + pl.off_rows), chain, s));
+    } else if (!fused) {
         if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
             constexpr int MB = 4, JB = 2;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));

@@ -61,19 +61,11 @@ struct TcDxParams {
     unsigned long long timeout_ns;
 };
 
-__device__ __forceinline__ int bx_exponent_offset(float s_t)
-{
-    int e = 0;
-    frexpf(s_t, &e);
-    const int c = 1 - e;
-    return c < 7 ? 7 : (c > 116 ? 116 : c);
-}
-__device__ __forceinline__ float bx_pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 // {f, f}, f = e4m3(b) * pow2 with b in bits 20..27 of b20 (see the forward).
 __device__ __forceinline__ uint32_t bx_scale(uint32_t b20, float pow2)
 {
-    const float f = __uint_as_float(b20 & 0x0FF00000u) * bx_pow2f(120) * pow2;
+    const float f = __uint_as_float(b20 & 0x0FF00000u) * pow2f(120) * pow2;
     const uint32_t u = __float_as_uint(f);
     return prmt(u, u, 0x3232u);
 }
@@ -245,7 +237,7 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
         // Thread: weight rows n = 2*lane, 2*lane + 1 of the step, columns
         // k = 32*warp .. +31 of the tile.
         const int n0l = 2 * lane, kw = 32 * warp;
-        const float pow2 = bx_pow2f(126 - bx_exponent_offset(*p.tensor_scale));
+        const float pow2 = pow2f(126 - tc_exponent_offset(*p.tensor_scale));
         for (int j = 0; j < n_total; ++j) {
             const int bs = j % BX_SB;
             if (j >= BX_SB && !__all_sync(0xFFFFFFFFu, wait(&b_empty[bs], (uint32_t)((j / BX_SB) - 1) & 1u))) break;
@@ -307,7 +299,7 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
             tc_fence_after();
             if (ok) {
                 const float st = *p.tensor_scale;
-                const float ysc = st * bx_pow2f(bx_exponent_offset(st));
+                const float ysc = st * pow2f(tc_exponent_offset(st));
                 const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
                 const int m = m0 + warp * 32 + lane;
                 __nv_bfloat16 *dst = p.dx + (size_t)m * p.K + k0;
@@ -348,7 +340,7 @@ __global__ void __launch_bounds__(256) vprime_kernel(const float *__restrict__ v
                                                      __nv_bfloat16 *__restrict__ vp)
 {
     const float st = *tensor_scale;
-    const float fac = s / (st * bx_pow2f(bx_exponent_offset(st)));
+    const float fac = s / (st * pow2f(tc_exponent_offset(st)));
     const int64_t total = (int64_t)M * r_pad;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t m = i / r_pad;
