@@ -33,37 +33,38 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64
     }
 }
 
-// z for channels 4i..4i+3; writes any of z_out / raw_out / scale_out given.
+// One thread per Box-Muller pair: thread 2i + p draws channels 4i + 2p and
+// 4i + 2p + 1 from Philox block i (both threads of a block compute it: the
+// FP64 transcendentals, not Philox, set the latency).  Writes any of z_out /
+// raw_out / scale_out given.
 __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32_t layer,
                                  const __nv_bfloat16 *__restrict__ gamma, float sigma, float *__restrict__ scale_out,
                                  float *__restrict__ z_out, uint64_t *__restrict__ raw_out)
 {
     pdl_trigger();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i * 4 >= H) return;
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = t >> 1;
+    const int p = (int)(t & 1);
+    if (4 * i + 2 * p >= H) return;
     uint64_t w[4] = {(uint64_t)i, step, 0ull, 0ull};
     philox4x64_10(w, seed, (uint64_t)layer);
-    double z[4];
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const double u1 = ((double)(w[2 * p] >> 11) + 1.0) * 0x1p-53;  // (0, 1]
-        const double u2 = (double)(w[2 * p + 1] >> 11) * 0x1p-53;      // [0, 1)
-        const double rad = sqrt(-2.0 * log(u1));
-        double sn, cs;
-        sincospi(2.0 * u2, &sn, &cs);
-        z[2 * p] = rad * cs;
-        z[2 * p + 1] = rad * sn;
-    }
+    const uint64_t w0 = p ? w[2] : w[0], w1 = p ? w[3] : w[1];
+    const double u1 = ((double)(w0 >> 11) + 1.0) * 0x1p-53;  // (0, 1]
+    const double u2 = (double)(w1 >> 11) * 0x1p-53;          // [0, 1)
+    const double rad = sqrt(-2.0 * log(u1));
+    double sn, cs;
+    sincospi(2.0 * u2, &sn, &cs);
+    const double z[2] = {rad * cs, rad * sn};
     // The draws need no input: only the writes (and gamma) wait for the
     // preceding work when the launch is chained.
     pdl_wait();
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const int64_t c = 4 * i + p;
+    for (int e = 0; e < 2; ++e) {
+        const int64_t c = 4 * i + 2 * p + e;
         if (c >= H) break;
-        if (z_out) z_out[c] = (float)z[p];
-        if (raw_out) raw_out[c] = w[p];
-        if (scale_out) scale_out[c] = (float)((double)bf16f(gamma[c]) + (double)sigma * z[p]);
+        if (z_out) z_out[c] = (float)z[e];
+        if (raw_out) raw_out[c] = e ? w1 : w0;
+        if (scale_out) scale_out[c] = (float)((double)bf16f(gamma[c]) + (double)sigma * z[e]);
     }
 }
 
@@ -155,7 +156,7 @@ extern "C" qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, u
     if (H < 1 || !z_out) return QERL_ERR_INVALID_ARG;
     QERL_TRY(check_device());
     const int64_t n = (H + 3) / 4;
-    aqn_noise_kernel<<<(unsigned)((n + 127) / 128), 128, 0, as_cuda(stream)>>>(H, seed, step, layer_id, nullptr,
+    aqn_noise_kernel<<<(unsigned)((2 * n + 63) / 64), 64, 0, as_cuda(stream)>>>(H, seed, step, layer_id, nullptr,
                                                                              0.0f, nullptr, z_out, raw_out);
     return launched();
 }
@@ -176,7 +177,7 @@ extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, con
     if (noisy) {
         gscale = static_cast<float *>(ws);
         const int64_t n = (H + 3) / 4;
-        QERL_TRY(launched(launch_k(aqn_noise_kernel, dim3((unsigned)((n + 127) / 128)), dim3(128), 0, s,
+        QERL_TRY(launched(launch_k(aqn_noise_kernel, dim3((unsigned)((2 * n + 63) / 64)), dim3(64), 0, s,
                                    g_chain.load() != 0, H, seed, step, layer_id,
                                    static_cast<const __nv_bfloat16 *>(gamma), sigma, gscale, (float *)nullptr,
                                    (uint64_t *)nullptr)));

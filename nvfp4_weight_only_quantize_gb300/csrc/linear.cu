@@ -242,6 +242,20 @@ __global__ void __launch_bounds__(256) simt_gemm(int64_t P, int64_t Q, int64_t K
         }
 }
 
+// sum_{z < splits} p[z * stride], in z order, eight loads in flight at a time.
+__device__ __forceinline__ float sum_splits(const float *p, int64_t stride, int splits)
+{
+    float acc = 0.0f;
+    for (int z0 = 0; z0 < splits; z0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = z0 + e < splits ? __ldcg(p + (int64_t)(z0 + e) * stride) : 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc += v[e];
+    }
+    return acc;
+}
+
 // Split-k partial: part[z][p][q] = acc.
 struct PartialEpi {
     float *part;
@@ -254,8 +268,7 @@ __global__ void __launch_bounds__(256) split_reduce(const float *__restrict__ pa
 {
     const int64_t n = P * Q;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        float v = 0.0f;
-        for (int z = 0; z < splits; ++z) v += part[z * n + i];
+        const float v = sum_splits(part + i, n, splits);
         float *o = out + (i / Q) * ld + (i % Q);
         *o = accumulate ? fmaf(alpha, v, *o) : alpha * v;
     }
@@ -562,7 +575,7 @@ __global__ void __launch_bounds__(256) u_reduce_kernel(const float *__restrict__
         const int j = (int)(i % r_pad);
         float t = 0.0f;
         if (j < r) {
-            for (int z = 0; z < splits; ++z) t += part[(z * M + m) * r + j];
+            t = sum_splits(part + m * r + j, M * r, splits);
             if (t_out) t_out[m * r + j] = t;
         }
         u[i] = __float2bfloat16_rn(t * fac);

@@ -710,13 +710,18 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
         const int m = m_tile * BN + col, n = n_tile * TILE_N + rq;
         if (m >= M || n >= N) continue;
         const float *base = partial + (size_t)tile * splits * (size_t)(TILE_N * BN) + (size_t)col * TILE_N + rq;
+        float4 v[MAX_SPLITS];  // every load in flight before the (fixed-order) sum
+#pragma unroll
+        for (int s2 = 0; s2 < MAX_SPLITS; ++s2)
+            v[s2] = s2 < splits ? __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN)))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s2 = 0; s2 < splits; ++s2) {  // fixed split order
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)s2 * (TILE_N * BN)));
-            a.x += v.x;
-            a.y += v.y;
-            a.z += v.z;
-            a.w += v.w;
+#pragma unroll
+        for (int s2 = 0; s2 < MAX_SPLITS; ++s2) {
+            a.x += v[s2].x;
+            a.y += v[s2].y;
+            a.z += v[s2].z;
+            a.w += v[s2].w;
         }
         __nv_bfloat16 *dst = y + (size_t)m * N + n;
         const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * ysc, a.y * ysc);
