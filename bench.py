@@ -142,6 +142,7 @@ class DecodeLayer:
         import nvfp4_weight_only_quantize_gb300 as q
         from nvfp4_weight_only_quantize_gb300 import synth
         self.q, self.wl, self.copies = q, wl, []
+        self.packed = packed
         self.fwd = q.qerl_nvfp4_lora_linear_fwd_packed if packed else q.qerl_nvfp4_lora_linear_fwd
         for c in range(n_copies):
             lins = []
@@ -164,32 +165,40 @@ class DecodeLayer:
         wl = self.wl
         outs = {name: torch.empty(M, N, dtype=torch.bfloat16, device=device) for name, N, K in wl.linears}
         ws_lin = max(self.q.workspace_bytes(self.q.OP_LINEAR_FWD, M, N, K, wl.r) for _, N, K in wl.linears)
+        Nof = {n: N for n, N, K in wl.linears}
+        for names in (("q_proj", "k_proj", "v_proj"), ("gate_proj", "up_proj")):
+            ws_lin = max(ws_lin, self.q.grouped_ws_bytes(M, wl.hidden, wl.r, [Nof[n] for n in names]))
         return dict(outs=outs, h1=torch.empty(M, wl.hidden, dtype=torch.bfloat16, device=device),
                     h2=torch.empty(M, wl.hidden, dtype=torch.bfloat16, device=device),
                     ws=torch.empty(max(ws_lin, 1), dtype=torch.uint8, device=device),
                     ws_norm=self.q.workspace(self.q.OP_AQN_RMSNORM, M, 0, wl.hidden, 0, device))
 
-    def step(self, copy, x, attn, buf, sigma, step_idx, ev=None):
-        """One decoder layer; ev: optional dict name -> list of (start, end) events."""
+    def step(self, copy, x, attn, buf, sigma, step_idx):
+        """One decoder layer: norm -> q|k|v (one grouped call) -> o -> norm ->
+        gate|up (one grouped call) -> down.  Attention and SwiGLU are not part
+        of this step (synthetic attention output; down reads up's output)."""
         q = self.q
         lins, gammas = self.copies[copy]
+        by = {l[0]: l for l in lins}
         o = buf["outs"]
+        s = self.wl.lora_scale
+
+        def group(names, xin):
+            gs = [by[n][3:8] for n in names]
+            q.qerl_nvfp4_lora_linear_fwd_grouped(xin, gs, s, packed=self.packed, ys=[o[n] for n in names],
+                                                 ws=buf["ws"])
+
+        def single(name, xin):
+            _, N, K, codes, scales, ts, A, B = by[name]
+            self.fwd(xin, codes, scales, ts, A, B, s, y=o[name], ws=buf["ws"])
+
         q.qerl_aqn_rmsnorm(x, gammas[0], 1e-6, sigma, 1, step_idx, 2 * copy, y=buf["h1"], ws=buf["ws_norm"])
-        src = {"q_proj": buf["h1"], "k_proj": buf["h1"], "v_proj": buf["h1"], "o_proj": attn}
-        for name, N, K, codes, scales, ts, A, B in lins:
-            if name == "gate_proj":
-                q.qerl_aqn_rmsnorm(o["o_proj"], gammas[1], 1e-6, sigma, 1, step_idx, 2 * copy + 1, y=buf["h2"],
-                                   ws=buf["ws_norm"])
-                src["gate_proj"] = src["up_proj"] = buf["h2"]
-                src["down_proj"] = o["up_proj"]
-            e0 = e1 = None
-            if ev is not None:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-            self.fwd(src[name], codes, scales, ts, A, B, self.wl.lora_scale, y=o[name], ws=buf["ws"])
-            if ev is not None:
-                e1.record()
-                ev.setdefault(name, []).append((e0, e1))
+        group(("q_proj", "k_proj", "v_proj"), buf["h1"])
+        single("o_proj", attn)
+        q.qerl_aqn_rmsnorm(o["o_proj"], gammas[1], 1e-6, sigma, 1, step_idx, 2 * copy + 1, y=buf["h2"],
+                           ws=buf["ws_norm"])
+        group(("gate_proj", "up_proj"), buf["h2"])
+        single("down_proj", o["up_proj"])
         return o["down_proj"]
 
 
@@ -319,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
                    "layer_copies_rotated": n_copies,
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies, "
                          f"{n_copies * per_copy / 2**20:.0f} MiB NVFP4 > 129 MiB L2",
-                   "launch": "one CUDA graph per step (per weight copy)",
+                   "launch": "one CUDA graph per step (per weight copy); q|k|v and gate|up as grouped calls",
                    "codes": args.codes + " layout (packed once when the weights are loaded)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(M * args.steps * world / max_secs, 1),

@@ -223,6 +223,33 @@ qerl_status qerl_nvfp4_unpack_codes(const uint8_t *packed, int64_t N, int64_t K,
                                     qerl_stream_t stream);
 
 /*
+ * Grouped forward: several linears that read the same x (in a decoder layer,
+ * q|k|v and gate|up read one normalised input) in one call; the same result as
+ * qerl_nvfp4_lora_linear_fwd (or _packed) on each group.  The pages have no
+ * such call: it is an interface of this library that saves launches.  For
+ * decode batches (M <= 64) the tensor-core path serves up to 3 groups in one
+ * launch; other shapes run the groups one after the other.
+ *   groups (host) [n_groups], 1 <= n_groups <= 8: per group N, codes, scales,
+ *   tensor_scale, A [r, K], B [N, r], y [M, N] out, t_out optional [M, r].
+ *   x (device) bf16 [M, K]; r, lora_scale and packed (0: standard codes,
+ *   1: packed layout) shared.  ws (device) >= qerl_lora_linear_fwd_grouped_ws_bytes.
+ */
+typedef struct qerl_lora_linear_group {
+    int64_t N;
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const float *tensor_scale;
+    const void *A;
+    const void *B;
+    void *y;
+    float *t_out;
+} qerl_lora_linear_group;
+size_t qerl_lora_linear_fwd_grouped_ws_bytes(int64_t M, int64_t K, int r, const int64_t *N, int n_groups);
+qerl_status qerl_nvfp4_lora_linear_fwd_grouped(const void *x, int64_t M, int64_t K, int r, float lora_scale,
+                                               const qerl_lora_linear_group *groups, int n_groups, int packed,
+                                               void *ws, size_t ws_bytes, qerl_stream_t stream);
+
+/*
  * qerl_nvfp4_lora_linear_fwd and qerl_nvfp4_lora_linear_bwd with the codes in
  * the packed layout above: same arguments, same results, same workspace sizes.
  */

@@ -33,7 +33,8 @@ EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_lin
             "qerl_nvfp4_lora_linear_fwd_packed", "qerl_nvfp4_lora_linear_bwd_packed",
             "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_noise", "qerl_aqn_sigma",
             "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
-            "qerl_set_launch_chaining",
+            "qerl_set_launch_chaining", "qerl_lora_linear_fwd_grouped_ws_bytes",
+            "qerl_nvfp4_lora_linear_fwd_grouped",
             "qerl_launch_count"]
 
 
@@ -88,6 +89,8 @@ def lib() -> C.CDLL:
                 "qerl_set_launch_chaining": ([i32], i32),
                 "qerl_launch_count": ([], u64),
             }
+            sig["qerl_lora_linear_fwd_grouped_ws_bytes"] = ([i64, i64, i32, vp, i32], sz)
+            sig["qerl_nvfp4_lora_linear_fwd_grouped"] = ([vp, i64, i64, i32, f32, vp, i32, i32, vp, sz, vp], i32)
             sig["qerl_nvfp4_lora_linear_fwd_packed"] = sig["qerl_nvfp4_lora_linear_fwd"]
             sig["qerl_nvfp4_lora_linear_bwd_packed"] = sig["qerl_nvfp4_lora_linear_bwd"]
             for name, (args, res) in sig.items():
@@ -189,6 +192,35 @@ def qerl_nvfp4_lora_linear_fwd_packed(x, packed_codes, scales, tensor_scale, A, 
     """The forward with the codes in the packed layout (qerl_nvfp4_pack_codes)."""
     return _fwd("qerl_nvfp4_lora_linear_fwd_packed", x, packed_codes, scales, tensor_scale, A, B, lora_scale, y,
                 t_out, ws, stream)
+
+
+class _Group(C.Structure):
+    _fields_ = [("N", C.c_int64), ("codes", C.c_void_p), ("scales", C.c_void_p), ("tensor_scale", C.c_void_p),
+                ("A", C.c_void_p), ("B", C.c_void_p), ("y", C.c_void_p), ("t_out", C.c_void_p)]
+
+
+def grouped_ws_bytes(M: int, K: int, r: int, Ns) -> int:
+    arr = (C.c_int64 * len(Ns))(*Ns)
+    return lib().qerl_lora_linear_fwd_grouped_ws_bytes(M, K, r, C.cast(arr, C.c_void_p), len(Ns))
+
+
+def qerl_nvfp4_lora_linear_fwd_grouped(x, groups, lora_scale: float, packed: bool = False, ys=None, t_outs=None,
+                                       ws=None, stream=None):
+    """Linears sharing x: groups = [(codes, scales, tensor_scale, A, B), ...].  Returns [y_g]."""
+    M, K = x.shape
+    r = groups[0][3].shape[0]
+    Ns = [g[4].shape[0] for g in groups]
+    ys = [torch.empty(M, N, dtype=torch.bfloat16, device=x.device) for N in Ns] if ys is None else ys
+    t_outs = [None] * len(groups) if t_outs is None else t_outs
+    arr = (_Group * len(groups))()
+    for i, (codes, scales, ts, A, B) in enumerate(groups):
+        arr[i] = _Group(Ns[i], _p(codes), _p(scales), _p(ts), _p(A), _p(B), _p(ys[i]), _p(t_outs[i]))
+    if ws is None:
+        ws = torch.empty(max(grouped_ws_bytes(M, K, r, Ns), 1), dtype=torch.uint8, device=x.device)
+    _check(lib().qerl_nvfp4_lora_linear_fwd_grouped(_p(x), M, K, r, float(lora_scale), C.cast(arr, C.c_void_p),
+                                                    len(groups), int(bool(packed)), _p(ws), ws.numel(),
+                                                    _stream(stream)), "qerl_nvfp4_lora_linear_fwd_grouped")
+    return ys
 
 
 def qerl_nvfp4_pack_codes(codes, out=None, stream=None):

@@ -836,3 +836,51 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_bwd_packed(const void *dy, const v
     return bwd_entry(dy, x, M, K, N, packed_codes, scales, tensor_scale, A, B, r, lora_scale, t_saved, dx, dA, dB,
                      accumulate_grads, ws, ws_bytes, stream, 1);
 }
+
+extern "C" size_t qerl_lora_linear_fwd_grouped_ws_bytes(int64_t M, int64_t K, int r, const int64_t *N, int n_groups)
+{
+    if (!N || n_groups < 1 || n_groups > 8 || M < 0 || K < 0 || r < 0) return 0;
+    size_t b = n_groups <= 3 ? tc_fwd_groups_ws_bytes(M, N, n_groups, K, r) : 0;
+    for (int g = 0; g < n_groups; ++g) b = std::max(b, linear_fwd_ws_bytes(M, N[g], K, r));
+    return b;
+}
+
+extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_grouped(const void *x, int64_t M, int64_t K, int r, float lora_scale,
+                                                          const qerl_lora_linear_group *groups, int n_groups,
+                                                          int packed, void *ws, size_t ws_bytes, qerl_stream_t stream)
+{
+    if (!groups || n_groups < 1 || n_groups > 8 || (packed != 0 && packed != 1)) return QERL_ERR_INVALID_ARG;
+    for (int g = 0; g < n_groups; ++g) {
+        const qerl_lora_linear_group &q = groups[g];
+        QERL_TRY(check_common(M, K, q.N, q.codes, q.scales, q.tensor_scale, q.A, q.B, r));
+        if (M > 0 && !q.y) return QERL_ERR_INVALID_ARG;
+        if ((q.y && !aligned16(q.y)) || (q.t_out && !aligned16(q.t_out))) return QERL_ERR_ALIGN;
+    }
+    if (M == 0) return QERL_OK;
+    if (!x) return QERL_ERR_INVALID_ARG;
+    if (!aligned16(x)) return QERL_ERR_ALIGN;
+    int64_t Ns[8];
+    for (int g = 0; g < n_groups; ++g) Ns[g] = groups[g].N;
+    if (!ws || ws_bytes < qerl_lora_linear_fwd_grouped_ws_bytes(M, K, r, Ns, n_groups)) return QERL_ERR_WORKSPACE;
+    QERL_TRY(check_device());
+    FwdArgs a[8];
+    for (int g = 0; g < n_groups; ++g) {
+        const qerl_lora_linear_group &q = groups[g];
+        a[g] = FwdArgs{static_cast<const __nv_bfloat16 *>(x), M, K, q.N, q.codes, q.scales, q.tensor_scale,
+                       static_cast<const __nv_bfloat16 *>(q.A), static_cast<const __nv_bfloat16 *>(q.B), r,
+                       lora_scale, static_cast<__nv_bfloat16 *>(q.y), q.t_out, packed};
+    }
+    cudaStream_t s = as_cuda(stream);
+    char *w = static_cast<char *>(ws);
+    if (g_algo.load() != QERL_ALGO_SIMT && n_groups > 1 && n_groups <= 3) {
+        const qerl_status st = tc_fwd_groups(a, n_groups, w, ws_bytes, s);
+        if (st != QERL_ERR_SHAPE) return st;
+    }
+    for (int g = 0; g < n_groups; ++g) {  // one group after the other
+        qerl_status st = QERL_ERR_SHAPE;
+        if (g_algo.load() != QERL_ALGO_SIMT) st = tc_linear_fwd(a[g], w, ws_bytes, s);
+        if (st == QERL_ERR_SHAPE) st = simt_fwd(a[g], w, s);
+        QERL_TRY(st);
+    }
+    return QERL_OK;
+}

@@ -43,6 +43,9 @@ size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 // when it does not cover the call; the caller then runs the CUDA-core path.
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s);
+// G (<= 3) linears sharing x, M, K, r, lora_scale and layout in one launch.
+qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, cudaStream_t s);
+size_t tc_fwd_groups_ws_bytes(int64_t M, const int64_t *N, int G, int64_t K, int r);
 
 inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 

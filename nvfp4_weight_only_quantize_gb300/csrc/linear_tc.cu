@@ -101,17 +101,31 @@ struct Cfg {
     static_assert(XS * X_STAGE >= BN * TILE_N * 2, "the y staging tile reuses the token ring");
 };
 
+// Up to MAX_GROUPS linears sharing x (and K, r, s): group g owns the weight
+// tiles [tile_start[g], tile_start[g + 1]) of the launch.
+constexpr int MAX_GROUPS = 3;
+struct TcGroups {
+    int G;
+    int tile_start[MAX_GROUPS + 1];
+    int N[MAX_GROUPS];
+    const __nv_bfloat16 *Bl[MAX_GROUPS];
+    const float *ts[MAX_GROUPS];
+    __nv_bfloat16 *y[MAX_GROUPS];
+};
+// Tensor maps of a launch: per group codes, scales, LoRA A (fused) and u
+// (unfused); x is shared.
+struct TcMaps {
+    CUtensorMap codes[MAX_GROUPS], scl[MAX_GROUPS], al[MAX_GROUPS], u[MAX_GROUPS], x;
+};
+
 struct TcFwdParams {
-    int M, N, K;
+    int M, K;
     int nk;              // K / BK main steps
     int lora_steps;      // ceil(r / BK)
     int r, r_pad;        // rank, u row length (lora_steps * BK)
     int splits, steps_per_split;
-    int n_tiles, m_tiles;
-    const uint8_t *scales;
-    const __nv_bfloat16 *Bl;
-    const float *tensor_scale;
-    __nv_bfloat16 *y;
+    int n_tiles, m_tiles;  // weight tiles over all groups, token tiles
+    TcGroups grp;
     float *partial;
     unsigned int *err;
     unsigned long long timeout_ns;
@@ -175,9 +189,7 @@ __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
 
 template <int BN, bool PACKED, bool FUSED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    tc_fwd_kernel(const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap x_map,
-                  const __grid_constant__ CUtensorMap u_map, const __grid_constant__ CUtensorMap scl_map,
-                  const __grid_constant__ CUtensorMap al_map, const TcFwdParams p)
+    tc_fwd_kernel(const __grid_constant__ TcMaps maps, const TcFwdParams p)
 {
     using C = Cfg<BN, FUSED>;
     constexpr int SPS = C::SPS;
@@ -210,7 +222,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int m_tile = (blockIdx.x / p.n_tiles) % p.m_tiles;
     const int split = blockIdx.x / (p.n_tiles * p.m_tiles);
     const int tile = m_tile * p.n_tiles + n_tile;
-    const int n0 = n_tile * TILE_N, m0 = m_tile * BN;
+    // the group (linear) this weight tile belongs to
+    int g = 0;
+#pragma unroll
+    for (int i = 1; i < MAX_GROUPS; ++i)
+        if (i < p.grp.G && n_tile >= p.grp.tile_start[i]) g = i;
+    const int Ng = p.grp.N[g];
+    const float *tsg = p.grp.ts[g];
+    const __nv_bfloat16 *Blg = p.grp.Bl[g];
+    __nv_bfloat16 *yg = p.grp.y[g];
+    const CUtensorMap *codes_map = &maps.codes[g], *scl_map = &maps.scl[g], *al_map = &maps.al[g];
+    const CUtensorMap *u_map = &maps.u[g], *x_map = &maps.x;
+    const int n0 = (n_tile - p.grp.tile_start[g]) * TILE_N, m0 = m_tile * BN;
     const int k_begin = split * p.steps_per_split;  // a multiple of GK
     const int k_end = min(p.nk, k_begin + p.steps_per_split);
     const int n_main = k_end > k_begin ? k_end - k_begin : 0;  // a multiple of GK (K % 256 == 0)
@@ -253,15 +276,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_mbar_init();
     }
     if (warp == WARP_RAW && lane == 0) {
-        prefetch_tensormap(&codes_map);
-        prefetch_tensormap(&scl_map);
+        prefetch_tensormap(codes_map);
+        prefetch_tensormap(scl_map);
     }
     if (warp == WARP_X && lane == 0) {
-        prefetch_tensormap(&x_map);
+        prefetch_tensormap(x_map);
         if (FUSED)
-            prefetch_tensormap(&al_map);
+            prefetch_tensormap(al_map);
         else
-            prefetch_tensormap(&u_map);
+            prefetch_tensormap(u_map);
     }
     if (warp == WARP_MMA) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -313,8 +336,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive_expect_tx(&raw_full[slot], RAW_STAGE);
                 const int kk = kstep(g * GK);  // first k-step of the group
                 uint8_t *dst = R_ring + slot * RAW_STAGE;
-                tma_load_2d_hint(dst, &codes_map, &raw_full[slot], kk * (BK / 2), n0, pol);
-                tma_load_2d_hint(dst + RAW_CODES, &scl_map, &raw_full[slot], kk * (BK / 16), n0, pol);
+                tma_load_2d_hint(dst, codes_map, &raw_full[slot], kk * (BK / 2), n0, pol);
+                tma_load_2d_hint(dst + RAW_CODES, scl_map, &raw_full[slot], kk * (BK / 16), n0, pol);
                 issued = g + 1;
             }
             if (*abort_flag)  // let the copies already issued land before the CTA exits
@@ -333,7 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (ok && round > 0) ok = __all_sync(0xFFFFFFFFu, wait(&x_empty[slot], (round - 1) & 1u));
             if (ok) {
                 tc_fence_after();
-                const float st = *p.tensor_scale;
+                const float st = *tsg;
                 const float fac = p.lora_scale / (st * pow2f(tc_exponent_offset(st)));
                 const uint32_t sdst = smem_u32(X_ring + slot * C::X_STAGE);
                 const bool jv = lane < p.r;
@@ -383,7 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int sub = 0; sub < SPS; ++sub) {
                         if (sub >= nsub) break;
-                        tma_load_2d_hint(AL_ring + slot * C::AL_STAGE + sub * C::AL_STEP, &al_map, &x_full[slot],
+                        tma_load_2d_hint(AL_ring + slot * C::AL_STAGE + sub * C::AL_STEP, al_map, &x_full[slot],
                                          kstep(j * SPS + sub) * BK, 0, pol);
                     }
                 }
@@ -391,7 +414,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int sub = 0; sub < SPS; ++sub) {
                     if (sub >= nsub) break;
                     const int i = j * SPS + sub;
-                    const CUtensorMap *map = i < n_main ? &x_map : &u_map;
+                    const CUtensorMap *map = i < n_main ? x_map : u_map;
                     const int kx = i < n_main ? kstep(i) * BK : (i - n_main) * BK;
                     if (cs == 1)
                         tma_load_2d_hint(dst + sub * C::X_STEP, map, &x_full[slot], kx, m0, pol);
@@ -463,8 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = (warp & 3) * 32 + lane;
         const int group = warp >> 2;
         const int n = n0 + row;
-        const bool row_ok = n < p.N;
-        const float pow2 = pow2f(126 - tc_exponent_offset(*p.tensor_scale));
+        const bool row_ok = n < Ng;
+        const float pow2 = pow2f(126 - tc_exponent_offset(*tsg));
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         for (int j = group; j < n_stages; j += DQ_GROUPS) {
             const int s = j % C::S;
@@ -506,7 +529,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // (Chained: B may be written by work before this call.)
                     if (p.chain) pdl_wait();
                     const int j0 = (i - n_main) * BK;
-                    const __nv_bfloat16 *b = p.Bl + (size_t)(row_ok ? n : 0) * p.r + j0;
+                    const __nv_bfloat16 *b = Blg + (size_t)(row_ok ? n : 0) * p.r + j0;
                     if (row_ok && (p.r & 7) == 0 && j0 + 64 <= p.r) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
@@ -549,7 +572,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             asm volatile("griddepcontrol.wait;" ::: "memory");  // the workspace and y follow the predecessor
             if (ok) {
-                const float st = *p.tensor_scale;
+                const float st = *tsg;
                 const float ysc = st * pow2f(tc_exponent_offset(st));
                 const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
                 if (p.splits == 1) {
@@ -564,17 +587,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             reinterpret_cast<__nv_bfloat16 *>(Y)[(c0 + j) * TILE_N + row] = __float2bfloat16_rn(v[j] * ysc);
                     }
                     named_bar_sync(1, 128);
-                    const bool vec = (p.N % 8) == 0;
+                    const bool vec = (Ng % 8) == 0;
                     for (int v = threadIdx.x; v < BN * (TILE_N / 8); v += 128) {
                         const int m = m0 + v / (TILE_N / 8), nn = n0 + (v % (TILE_N / 8)) * 8;
-                        if (m >= p.M || nn >= p.N) continue;
+                        if (m >= p.M || nn >= Ng) continue;
                         const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(Y) +
                                                    (v / (TILE_N / 8)) * TILE_N + (v % (TILE_N / 8)) * 8;
-                        __nv_bfloat16 *dst = p.y + (size_t)m * p.N + nn;
-                        if (vec && nn + 8 <= p.N) {
+                        __nv_bfloat16 *dst = yg + (size_t)m * Ng + nn;
+                        if (vec && nn + 8 <= Ng) {
                             *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
                         } else {
-                            for (int e = 0; e < 8 && nn + e < p.N; ++e) dst[e] = src[e];
+                            for (int e = 0; e < 8 && nn + e < Ng; ++e) dst[e] = src[e];
                         }
                     }
                 } else {
@@ -692,14 +715,10 @@ __global__ void __launch_bounds__(LD_THREADS)
 // thread per four rows n of one token m (16-byte partial loads).  Chained
 // after the main kernel: it waits for that grid before reading.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ partial, int splits, int n_tiles,
-                                                            int m_tiles, int BN, int M, int N,
-                                                            const float *__restrict__ tensor_scale,
-                                                            __nv_bfloat16 *__restrict__ y)
+                                                            int m_tiles, int BN, int M, const TcGroups grp)
 {
     pdl_trigger();
     pdl_wait();
-    const float st = *tensor_scale;
-    const float ysc = st * pow2f(tc_exponent_offset(st));
     const int64_t items = (int64_t)n_tiles * m_tiles * BN * (TILE_N / 4);
     for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (int64_t)gridDim.x * blockDim.x) {
         const int rq = (int)(it % (TILE_N / 4)) * 4;
@@ -707,8 +726,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
         const int col = (int)(rest % BN);
         const int64_t tile = rest / BN;  // m_tile * n_tiles + n_tile
         const int n_tile = (int)(tile % n_tiles), m_tile = (int)(tile / n_tiles);
-        const int m = m_tile * BN + col, n = n_tile * TILE_N + rq;
+        int g = 0;
+#pragma unroll
+        for (int i = 1; i < MAX_GROUPS; ++i)
+            if (i < grp.G && n_tile >= grp.tile_start[i]) g = i;
+        const int N = grp.N[g];
+        const int m = m_tile * BN + col, n = (n_tile - grp.tile_start[g]) * TILE_N + rq;
         if (m >= M || n >= N) continue;
+        const float st = *grp.ts[g];
+        const float ysc = st * pow2f(tc_exponent_offset(st));
         const float *base = partial + (size_t)tile * splits * (size_t)(TILE_N * BN) + (size_t)col * TILE_N + rq;
         float4 v[MAX_SPLITS];  // every load in flight before the (fixed-order) sum
 #pragma unroll
@@ -723,7 +749,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
             a.z += v[s2].z;
             a.w += v[s2].w;
         }
-        __nv_bfloat16 *dst = y + (size_t)m * N + n;
+        __nv_bfloat16 *dst = grp.y[g] + (size_t)m * N + n;
         const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * ysc, a.y * ysc);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * ysc, a.w * ysc);
         if ((N & 3) == 0 && n + 4 <= N) {
@@ -742,14 +768,18 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
 
 struct FwdPlan {
     int BN = 0, n_tiles = 0, m_tiles = 0, splits = 1, sps = 0, nk = 0, lora_steps = 0, r_pad = 0;
-    size_t off_u = 0, off_part = 0, off_rows = 0, total = 0;
+    size_t u_bytes = 0, off_u = 0, off_part = 0, off_rows = 0, total = 0;
 };
 
-FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
+// Launch plan for G linears sharing x: their weight tiles side by side, one
+// split factor, one u region per group, the split partials, and (one linear,
+// many tokens) the partials of the rows x rank down-projection.
+FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r)
 {
     FwdPlan pl;
     pl.BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-    pl.n_tiles = (int)((N + TILE_N - 1) / TILE_N);
+    pl.n_tiles = 0;
+    for (int g = 0; g < G; ++g) pl.n_tiles += (int)((N[g] + TILE_N - 1) / TILE_N);
     pl.m_tiles = (int)((M + pl.BN - 1) / pl.BN);
     pl.nk = (int)(K / BK);
     pl.lora_steps = (r + BK - 1) / BK;
@@ -767,11 +797,12 @@ FwdPlan plan_fwd(int64_t M, int64_t N, int64_t K, int r)
     pl.sps = (pl.nk + splits - 1) / splits;
     pl.sps = (pl.sps + GK - 1) / GK * GK;  // splits start on a raw-stage boundary
     pl.splits = (pl.nk + pl.sps - 1) / pl.sps;  // no empty split
+    pl.u_bytes = round256(size_t(M) * pl.r_pad * 2);
     pl.off_u = 0;
-    pl.off_part = round256(size_t(M) * pl.r_pad * 2);
+    pl.off_part = pl.u_bytes * G;
     pl.off_rows = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
     // many tokens: the down-projection runs as a split-K rows x rank product
-    pl.total = pl.off_rows + (M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r) : 0);
+    pl.total = pl.off_rows + (G == 1 && M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r) : 0);
     return pl;
 }
 
@@ -849,9 +880,7 @@ int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int n_tiles, unsigned gr
 }
 
 template <int BN, bool FUSED>
-qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUtensorMap &um, const CUtensorMap &sm,
-                       const CUtensorMap &alm, const TcFwdParams &p0, unsigned grid, bool packed, bool pdl,
-                       cudaStream_t s)
+qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid, bool packed, bool pdl, cudaStream_t s)
 {
     using C = Cfg<BN, FUSED>;
     auto kernel = packed ? tc_fwd_kernel<BN, true, FUSED> : tc_fwd_kernel<BN, false, FUSED>;
@@ -879,7 +908,7 @@ qerl_status launch_fwd(const CUtensorMap &cm, const CUtensorMap &xm, const CUten
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kernel, cm, xm, um, sm, alm, p) != cudaSuccess) return QERL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess) return QERL_ERR_CUDA;
     return launched();
 }
 
@@ -916,66 +945,84 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
 
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {
-    return tc_fwd_applies(M, N, K, r) ? plan_fwd(M, N, K, r).total : 0;
+    return tc_fwd_applies(M, N, K, r) ? plan_fwd(M, &N, 1, K, r).total : 0;
 }
 
-qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s)
+// G linears sharing x, M, K, r, lora_scale and the code layout (G = 1: one
+// linear).  Returns QERL_ERR_SHAPE, having launched nothing, when the shapes
+// are not covered.
+qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, cudaStream_t s)
 {
-    if (!tc_fwd_applies(a.M, a.N, a.K, a.r)) return QERL_ERR_SHAPE;
-    const FwdPlan pl = plan_fwd(a.M, a.N, a.K, a.r);
+    if (G < 1 || G > MAX_GROUPS) return QERL_ERR_SHAPE;
+    const FwdArgs &a = ga[0];
+    int64_t Ns[MAX_GROUPS];
+    bool any_t = false;
+    for (int g = 0; g < G; ++g) {
+        if (!tc_fwd_applies(a.M, ga[g].N, a.K, a.r)) return QERL_ERR_SHAPE;
+        Ns[g] = ga[g].N;
+        any_t = any_t || ga[g].t_out;
+    }
+    const FwdPlan pl = plan_fwd(a.M, Ns, G, a.K, a.r);
+    if (G > 1 && a.M > 64) return QERL_ERR_SHAPE;  // grouping serves decode tiles
     if (ws_bytes < pl.total) return QERL_ERR_WORKSPACE;
-    __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u);
     float *partial = reinterpret_cast<float *>(ws + pl.off_part);
     const int tiles = pl.n_tiles * pl.m_tiles;
 
-    // Fused LoRA down-projection (no separate grid) for decode tiles split over
-    // K when t is not requested.  Unsplit linears keep the separate grid: it
-    // overlaps their long weight stream, while the fused MMAs would load it.
-    const bool fused = !a.t_out && pl.BN <= 64 && a.r <= FUSED_R && pl.splits > 1 && !env().no_fuse;
-    CUtensorMap cm, xm, um, sm, alm;
+    // Fused LoRA down-projection (no separate grid) for decode tiles when t is
+    // not requested, for split launches and for groups.  A single unsplit
+    // linear keeps the separate grid: it overlaps the long weight stream, while
+    // the fused MMAs would load it.
+    const bool fused = !any_t && pl.BN <= 64 && a.r <= FUSED_R && (pl.splits > 1 || G > 1) && !env().no_fuse;
+    TcMaps maps;
     // codes: 128 rows x 128 bytes (4 k-steps) per box, 128-byte swizzle; scales:
     // 128 rows x 16 bytes (the same 4 k-steps); token tiles: BN rows x 64 bf16;
     // fused: LoRA A rows 0..31 x 64 bf16 (zero past r).
-    if (!make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, a.K / 2, a.N, a.K / 2, GK * BK / 2, TILE_N,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&sm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, a.K / 16, a.N, a.K / 16, GK * BK / 16, TILE_N,
-                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, a.K * 2, BK, pl.BN,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&um, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, pl.r_pad, a.M, pl.r_pad * 2, BK, pl.BN,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&alm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.A, a.K, a.r, a.K * 2, BK, FUSED_R,
+    if (!make_map_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, a.K * 2, BK, pl.BN,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return QERL_ERR_CUDA;
+    for (int g = 0; g < MAX_GROUPS; ++g) {
+        const FwdArgs &b = ga[g < G ? g : 0];  // unused slots repeat group 0
+        __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u + (g < G ? g : 0) * pl.u_bytes);
+        if (!make_map_2d(&maps.codes[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, b.codes, a.K / 2, b.N, a.K / 2, GK * BK / 2,
+                         TILE_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map_2d(&maps.scl[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, b.scales, a.K / 16, b.N, a.K / 16,
+                         GK * BK / 16, TILE_N, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map_2d(&maps.u[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, pl.r_pad, a.M, pl.r_pad * 2, BK, pl.BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map_2d(&maps.al[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.A, a.K, a.r, a.K * 2, BK, FUSED_R,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return QERL_ERR_CUDA;
+    }
 
-    // 1) LoRA down-projection (+ counter reset).  Chained, it may start before
-    //    the preceding work finishes (it waits for it before touching memory),
-    //    and the main kernel may then stream and dequantize its (frozen) weight
+    // 1) LoRA down-projection, unless fused.  Chained, it may start before the
+    //    preceding work finishes (it waits for it before touching memory), and
+    //    the main kernel may then stream and dequantize its (frozen) weight
     //    while that work is still running.
     const bool chain = g_chain.load() != 0;
-    if (!fused && a.M > 64 && lora_down_rows_applies(a.K, a.r)) {
-        QERL_TRY(lora_down_rows(a.x, a.M, a.K, a.A, a.r, pl.r_pad, a.lora_scale, a.tensor_scale, a.t_out, u,
-                                reinterpret_cast<float *>(ws + pl.off_rows), chain, s));
-    } else if (!fused) {
-        if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
+    for (int g = 0; g < G && !fused; ++g) {
+        const FwdArgs &b = ga[g];
+        __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u + g * pl.u_bytes);
+        if (a.M > 64 && lora_down_rows_applies(a.K, a.r)) {
+            QERL_TRY(lora_down_rows(a.x, a.M, a.K, b.A, a.r, pl.r_pad, a.lora_scale, b.tensor_scale, b.t_out, u,
+                                    reinterpret_cast<float *>(ws + pl.off_rows), chain, s));
+        } else if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
             constexpr int MB = 4, JB = 2;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
             QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
-                                       a.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, a.tensor_scale,
-                                       a.t_out, u)));
+                                       b.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, b.tensor_scale,
+                                       b.t_out, u)));
         } else {
             constexpr int MB = 8, JB = 4;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
             QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
-                                       a.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, a.tensor_scale,
-                                       a.t_out, u)));
+                                       b.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, b.tensor_scale,
+                                       b.t_out, u)));
         }
     }
 
     // 2) main tensor-core kernel
     TcFwdParams p;
     p.M = (int)a.M;
-    p.N = (int)a.N;
     p.K = (int)a.K;
     p.nk = pl.nk;
     p.lora_steps = pl.lora_steps;
@@ -985,10 +1032,18 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     p.steps_per_split = pl.sps;
     p.n_tiles = pl.n_tiles;
     p.m_tiles = pl.m_tiles;
-    p.scales = a.scales;
-    p.Bl = a.B;
-    p.tensor_scale = a.tensor_scale;
-    p.y = a.y;
+    p.grp.G = G;
+    int t0 = 0;
+    for (int g = 0; g < MAX_GROUPS; ++g) {
+        const FwdArgs &b = ga[g < G ? g : 0];
+        p.grp.tile_start[g] = t0;
+        if (g < G) t0 += (int)((b.N + TILE_N - 1) / TILE_N);
+        p.grp.N[g] = (int)b.N;
+        p.grp.Bl[g] = b.B;
+        p.grp.ts[g] = b.tensor_scale;
+        p.grp.y[g] = b.y;
+    }
+    p.grp.tile_start[MAX_GROUPS] = t0;
     p.partial = partial;
     p.err = error_word();
     p.timeout_ns = env().timeout_ns;
@@ -1002,27 +1057,37 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
     const bool pk = a.packed != 0, pdl = fused ? chain : true;
     switch (pl.BN) {
     case 16:
-        st = fused ? launch_fwd<16, true>(cm, xm, um, sm, alm, p, grid, pk, pdl, s)
-                   : launch_fwd<16, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s);
+        st = fused ? launch_fwd<16, true>(maps, p, grid, pk, pdl, s) : launch_fwd<16, false>(maps, p, grid, pk, pdl, s);
         break;
     case 32:
-        st = fused ? launch_fwd<32, true>(cm, xm, um, sm, alm, p, grid, pk, pdl, s)
-                   : launch_fwd<32, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s);
+        st = fused ? launch_fwd<32, true>(maps, p, grid, pk, pdl, s) : launch_fwd<32, false>(maps, p, grid, pk, pdl, s);
         break;
     case 64:
-        st = fused ? launch_fwd<64, true>(cm, xm, um, sm, alm, p, grid, pk, pdl, s)
-                   : launch_fwd<64, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s);
+        st = fused ? launch_fwd<64, true>(maps, p, grid, pk, pdl, s) : launch_fwd<64, false>(maps, p, grid, pk, pdl, s);
         break;
-    case 128: st = launch_fwd<128, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s); break;
-    default: st = launch_fwd<256, false>(cm, xm, um, sm, alm, p, grid, pk, pdl, s); break;
+    case 128: st = launch_fwd<128, false>(maps, p, grid, pk, pdl, s); break;
+    default: st = launch_fwd<256, false>(maps, p, grid, pk, pdl, s); break;
     }
     if (st != QERL_OK || pl.splits == 1) return st;
     // 3) split-K: sum the partial tiles (chained: waits for the main grid)
-    const int64_t items = tiles * pl.BN * (TILE_N / 4);
-    int64_t g = (items + 255) / 256;
-    if (g > 8 * num_sms()) g = 8 * num_sms();
-    return launched(launch_k(splitk_reduce_kernel, dim3((unsigned)g), dim3(256), 0, s, chain, (const float *)partial,
-                             pl.splits, pl.n_tiles, pl.m_tiles, pl.BN, (int)a.M, (int)a.N, a.tensor_scale, a.y));
+    const int64_t items = (int64_t)tiles * pl.BN * (TILE_N / 4);
+    int64_t gr = (items + 255) / 256;
+    if (gr > 8 * num_sms()) gr = 8 * num_sms();
+    return launched(launch_k(splitk_reduce_kernel, dim3((unsigned)gr), dim3(256), 0, s, chain, (const float *)partial,
+                             pl.splits, pl.n_tiles, pl.m_tiles, pl.BN, (int)a.M, p.grp));
+}
+
+size_t tc_fwd_groups_ws_bytes(int64_t M, const int64_t *N, int G, int64_t K, int r)
+{
+    if (G < 1 || G > MAX_GROUPS) return 0;
+    for (int g = 0; g < G; ++g)
+        if (!tc_fwd_applies(M, N[g], K, r)) return 0;
+    return plan_fwd(M, N, G, K, r).total;
+}
+
+qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s)
+{
+    return tc_fwd_groups(&a, 1, ws, ws_bytes, s);
 }
 
 }  // namespace qerl
