@@ -175,7 +175,7 @@ class DecodeLayer:
 
     def step(self, copy, x, attn, buf, sigma, step_idx):
         """One decoder layer: norm -> q|k|v (one grouped call) -> o -> norm ->
-        gate|up (one grouped call) -> down.  Attention and SwiGLU are not part
+        gate -> up -> down.  Attention and SwiGLU are not part
         of this step (synthetic attention output; down reads up's output)."""
         q = self.q
         lins, gammas = self.copies[copy]
@@ -197,7 +197,10 @@ class DecodeLayer:
         single("o_proj", attn)
         q.qerl_aqn_rmsnorm(o["o_proj"], gammas[1], 1e-6, sigma, 1, step_idx, 2 * copy + 1, y=buf["h2"],
                            ws=buf["ws_norm"])
-        group(("gate_proj", "up_proj"), buf["h2"])
+        # gate and up stay separate calls: grouped they need two waves of
+        # one-tile CTAs over the SMs, which measured slower than two launches
+        single("gate_proj", buf["h2"])
+        single("up_proj", buf["h2"])
         single("down_proj", o["up_proj"])
         return o["down_proj"]
 
@@ -328,7 +331,7 @@ def run_ours(args, rank, world, local_rank):
                    "layer_copies_rotated": n_copies,
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies, "
                          f"{n_copies * per_copy / 2**20:.0f} MiB NVFP4 > 129 MiB L2",
-                   "launch": "one CUDA graph per step (per weight copy); q|k|v and gate|up as grouped calls",
+                   "launch": "one CUDA graph per step (per weight copy); q|k|v as one grouped call",
                    "codes": args.codes + " layout (packed once when the weights are loaded)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(M * args.steps * world / max_secs, 1),
