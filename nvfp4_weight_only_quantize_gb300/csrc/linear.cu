@@ -363,22 +363,40 @@ __global__ void __launch_bounds__(256) thin_rows_kernel(const __nv_bfloat16 *__r
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
-    for (int64_t k0 = kbeg; k0 < kend; k0 += THIN_TK) {
-        // X: 128 rows x 32 k = 512 16-byte vectors (Kd % 8 == 0, chunks of 32 k)
-        for (int v = tid; v < THIN_TR * (THIN_TK / 8); v += 256) {
+    // The next chunk is loaded into registers while the current one is used.
+    constexpr int XV = THIN_TR * (THIN_TK / 8) / 256;  // 16-byte X vectors per thread
+    constexpr int WV = THIN_TK * 64 / 256;             // W values per thread
+    uint4 xr[XV];
+    float wr[WV];
+    auto load = [&](int64_t k0) {
+#pragma unroll
+        for (int e = 0; e < XV; ++e) {  // X: THIN_TR rows x 32 k (Kd % 8 == 0, chunks of 32 k)
+            const int v = tid + 256 * e;
             const int row = v / (THIN_TK / 8), kk = (v % (THIN_TK / 8)) * 8;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (m0 + row < M && k0 + kk < kend) u = __ldg(reinterpret_cast<const uint4 *>(X + (m0 + row) * Kd + k0 + kk));
-            *reinterpret_cast<uint4 *>(&Xs[row][kk]) = u;
+            xr[e] = (m0 + row < M && k0 + kk < kend) ? __ldg(reinterpret_cast<const uint4 *>(X + (m0 + row) * Kd + k0 + kk))
+                                                     : make_uint4(0, 0, 0, 0);
         }
-        // W: 32 k x r_pad ranks as FP32 (zeros past r and kend)
-        for (int i = tid; i < THIN_TK * 64; i += 256) {
+#pragma unroll
+        for (int e = 0; e < WV; ++e) {  // W: 32 k x 64 ranks as FP32 (zeros past r and kend)
+            const int i = tid + 256 * e;
             const int kk = WJK ? (i % THIN_TK) : (i / 64), j = WJK ? (i / THIN_TK) : (i % 64);
-            float w = 0.0f;
-            if (j < r && k0 + kk < kend) w = bf16f(WJK ? W[(int64_t)j * Kd + k0 + kk] : W[(k0 + kk) * r + j]);
-            Ws[kk][j] = w;
+            wr[e] = (j < r && k0 + kk < kend) ? bf16f(WJK ? W[(int64_t)j * Kd + k0 + kk] : W[(k0 + kk) * r + j]) : 0.0f;
+        }
+    };
+    if (kbeg < kend) load(kbeg);
+    for (int64_t k0 = kbeg; k0 < kend; k0 += THIN_TK) {
+#pragma unroll
+        for (int e = 0; e < XV; ++e) {
+            const int v = tid + 256 * e;
+            *reinterpret_cast<uint4 *>(&Xs[v / (THIN_TK / 8)][(v % (THIN_TK / 8)) * 8]) = xr[e];
+        }
+#pragma unroll
+        for (int e = 0; e < WV; ++e) {
+            const int i = tid + 256 * e;
+            Ws[WJK ? (i % THIN_TK) : (i / 64)][WJK ? (i / THIN_TK) : (i % 64)] = wr[e];
         }
         __syncthreads();
+        if (k0 + THIN_TK < kend) load(k0 + THIN_TK);
         if (active) {
 #pragma unroll
             for (int kk = 0; kk < THIN_TK; kk += 8) {
@@ -435,19 +453,40 @@ __global__ void __launch_bounds__(256) thin_wide_kernel(const __nv_bfloat16 *__r
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.0f;
-    for (int64_t mm0 = mbeg; mm0 < mend; mm0 += THIN_TK) {
-        // D: 32 m x 128 w = 512 16-byte vectors (Wd % 8 == 0)
-        for (int v = tid; v < THIN_TK * (THIN_TR / 8); v += 256) {
+    // The next chunk is loaded into registers while the current one is used.
+    constexpr int DV = THIN_TK * (THIN_TR / 8) / 256;  // 16-byte D vectors per thread
+    constexpr int TV = THIN_TK * 64 / 256;             // T values per thread
+    uint4 dr[DV];
+    float tr[TV];
+    auto load = [&](int64_t mm0) {
+#pragma unroll
+        for (int e = 0; e < DV; ++e) {  // D: 32 m x THIN_TR w (Wd % 8 == 0)
+            const int v = tid + 256 * e;
             const int mm = v / (THIN_TR / 8), ww = (v % (THIN_TR / 8)) * 8;
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (mm0 + mm < mend && w0 + ww < Wd) u = __ldg(reinterpret_cast<const uint4 *>(D + (mm0 + mm) * Wd + w0 + ww));
-            *reinterpret_cast<uint4 *>(&Ds[mm][ww]) = u;
+            dr[e] = (mm0 + mm < mend && w0 + ww < Wd) ? __ldg(reinterpret_cast<const uint4 *>(D + (mm0 + mm) * Wd + w0 + ww))
+                                                       : make_uint4(0, 0, 0, 0);
         }
-        for (int i = tid; i < THIN_TK * 64; i += 256) {
+#pragma unroll
+        for (int e = 0; e < TV; ++e) {
+            const int i = tid + 256 * e;
             const int mm = i / 64, j = i % 64;
-            Ts[mm][j] = (j < r && mm0 + mm < mend) ? T[(mm0 + mm) * r + j] : 0.0f;
+            tr[e] = (j < r && mm0 + mm < mend) ? T[(mm0 + mm) * r + j] : 0.0f;
+        }
+    };
+    if (mbeg < mend) load(mbeg);
+    for (int64_t mm0 = mbeg; mm0 < mend; mm0 += THIN_TK) {
+#pragma unroll
+        for (int e = 0; e < DV; ++e) {
+            const int v = tid + 256 * e;
+            *reinterpret_cast<uint4 *>(&Ds[v / (THIN_TR / 8)][(v % (THIN_TR / 8)) * 8]) = dr[e];
+        }
+#pragma unroll
+        for (int e = 0; e < TV; ++e) {
+            const int i = tid + 256 * e;
+            Ts[i / 64][i % 64] = tr[e];
         }
         __syncthreads();
+        if (mm0 + THIN_TK < mend) load(mm0 + THIN_TK);
         if (active) {
 #pragma unroll 8
             for (int mm = 0; mm < THIN_TK; ++mm) {
