@@ -3,8 +3,11 @@
 // (bitsofall "QeRL: NVFP4-Quantized Reinforcement Learning", "Implementation
 // and Practical Details": gradients flow through the dequantized frozen weight).
 //
-// One CTA computes a 128-token x 256-column tile of dx as D[m][k] (TMEM, FP32):
-//   A operand = dy tile [128 tokens x 64 n], K-major, loaded by TMA;
+// One CTA computes a 256-token x 256-column tile of dx as two accumulators
+// D0, D1 [128 tokens][256 columns] (TMEM, FP32, all 512 columns), so that each
+// dequantized weight tile serves 256 tokens:
+//   A operand = dy tile [256 tokens x 64 n] (one TMA box), K-major, each
+//               accumulator reading its 128-row half;
 //   B operand = w_hat^T tile [256 k x 64 n], K-major, written by the dequant
 //               warps straight from the packed codes (each thread owns two
 //               adjacent weight rows n, n+1 over 32 k, so that its shared-memory
@@ -32,16 +35,17 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BX_M = 128;   // tokens per tile (MMA M)
+constexpr int BX_M = 128;   // tokens per accumulator (MMA M)
+constexpr int BX_MT = 2;    // accumulators (token tiles) per CTA sharing each weight tile
 constexpr int BX_K = 256;   // dx columns per tile (MMA N)
 constexpr int BX_N = 64;    // reduction (weight rows n) per step
 constexpr int BX_THREADS = 320;
 constexpr int BX_WARP_TMA = 8, BX_WARP_MMA = 9;
 constexpr int BX_DQ_WARPS = 8;
-constexpr int BX_SA = 4;    // dy / v' stages
+constexpr int BX_SA = 2;    // dy / v' stages (256 tokens each)
 constexpr int BX_SB = 3;    // w_hat^T / A^T stages
 constexpr int BX_R = 4;     // raw (codes + scales) stages
-constexpr int BX_A_BYTES = BX_M * BX_N * 2;          // 16 KB
+constexpr int BX_A_BYTES = BX_MT * BX_M * BX_N * 2;  // 32 KB
 constexpr int BX_B_BYTES = BX_K * BX_N * 2;          // 32 KB
 constexpr int BX_CODES = BX_N * (BX_K / 2);          // 64 rows x 128 B = 8 KB
 constexpr int BX_RAW = BX_CODES + BX_N * (BX_K / 16);  // + 64 rows x 16 B of scales
@@ -121,7 +125,7 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // blockIdx.x = m_tile * k_tiles + k_tile: a wave shares its dy tiles (L2)
     const int k_tile = blockIdx.x % p.k_tiles, m_tile = blockIdx.x / p.k_tiles;
-    const int k0 = k_tile * BX_K, m0 = m_tile * BX_M;
+    const int k0 = k_tile * BX_K, m0 = m_tile * (BX_MT * BX_M);
     const int n_total = p.n_steps + p.lora_steps;
 
     if (threadIdx.x == 0) {
@@ -148,7 +152,7 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
         prefetch_tensormap(&scl_map);
     }
     if (warp == BX_WARP_MMA) {
-        tmem_alloc(tmem_slot, BX_K);
+        tmem_alloc(tmem_slot, BX_MT * BX_K);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -223,8 +227,11 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
                 const uint64_t ad = desc_kmajor_sw128(smem_u32(A_ring + as * BX_A_BYTES));
                 const uint64_t bd = desc_kmajor_sw128(smem_u32(B_ring + bs * BX_B_BYTES));
 #pragma unroll
-                for (int kk = 0; kk < BX_N / 16; ++kk)  // 16 n = 32 bytes of each K-major row
-                    umma_bf16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int t = 0; t < BX_MT; ++t)  // accumulator t: tokens 128 t .. 128 t + 127 (16 KB in)
+#pragma unroll
+                    for (int kk = 0; kk < BX_N / 16; ++kk)  // 16 n = 32 bytes of each K-major row
+                        umma_bf16(tmem + (uint32_t)(t * BX_K), ad + (uint64_t)((t * BX_M * 128) >> 4) + 2u * kk,
+                                  bd + 2u * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&a_empty[as]);
                 umma_commit(&b_empty[bs]);
             }
@@ -300,10 +307,11 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
             if (ok) {
                 const float st = *p.tensor_scale;
                 const float ysc = st * pow2f(tc_exponent_offset(st));
-                const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-                const int m = m0 + warp * 32 + lane;
-                __nv_bfloat16 *dst = p.dx + (size_t)m * p.K + k0;
-                for (int c0 = 0; c0 < BX_K; c0 += 16) {
+                for (int c = 0; c < BX_MT * BX_K; c += 16) {
+                    const int t = c / BX_K, c0 = c % BX_K;
+                    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(t * BX_K);
+                    const int m = m0 + t * BX_M + warp * 32 + lane;
+                    __nv_bfloat16 *dst = p.dx + (size_t)m * p.K + k0;
                     uint32_t r[16];
                     tmem_ld16(taddr + (uint32_t)c0, r);
                     tmem_wait_ld();
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(BX_THREADS, 1)
         if (lane == 0) drain_wait(acc_full, 0);  // every issued MMA has finished (no-op unless aborted)
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, BX_K);
+        tmem_dealloc(tmem, BX_MT * BX_K);
     }
 }
 
@@ -380,9 +388,9 @@ qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, cudaStream_t s)
     CUtensorMap dym, vm, cm, sm;
     // dy: [M, N] bf16, 64 x 128 boxes; v': [M, r_pad]; codes: 64 rows x 128 bytes
     // (256 columns), 128-byte swizzle; scales: 64 rows x 16 bytes.
-    if (!make_map_2d(&dym, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.dy, a.N, a.M, a.N * 2, BX_N, BX_M,
+    if (!make_map_2d(&dym, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.dy, a.N, a.M, a.N * 2, BX_N, BX_MT * BX_M,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, vp, r_pad, a.M, r_pad * 2, BX_N, BX_M,
+        !make_map_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, vp, r_pad, a.M, r_pad * 2, BX_N, BX_MT * BX_M,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, a.K / 2, a.N, a.K / 2, BX_K / 2, BX_N,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -403,7 +411,7 @@ qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, cudaStream_t s)
     p.err = error_word();
     static const BxEnv env;
     p.timeout_ns = env.timeout_ns;
-    const int64_t m_tiles = (a.M + BX_M - 1) / BX_M;
+    const int64_t m_tiles = (a.M + BX_MT * BX_M - 1) / (BX_MT * BX_M);
     const int64_t grid = m_tiles * p.k_tiles;
     if (grid > 0x7FFFFFFF) return QERL_ERR_SHAPE;
     auto kernel = a.packed ? tc_dx_kernel<true> : tc_dx_kernel<false>;
