@@ -415,6 +415,7 @@ def other_rows(dev, only=None, profile=False):
     # a4: Qwen2.5-14B prefill linears, M = 4096, r = 32
     wl = synth.WORKLOADS[2]
     M, tot_f, tot_s, per = 4096, 0.0, 0.0, {}
+    per_lin_args, per_lin_N, per_flops = {}, {}, {}
     _, bf16, _, kind = peaks()
     if not want("a4"):
         wl = synth.Workload(wl.name, [], wl.M, wl.r, wl.hidden)
@@ -433,9 +434,25 @@ def other_rows(dev, only=None, profile=False):
         fl = 2.0 * M * N * K + 2.0 * M * wl.r * (N + K)
         per[name] = {"us": round(sec * 1e6, 1), "TFLOPs": round(fl / sec / 1e12, 1)}
         tot_f, tot_s = tot_f + fl, tot_s + sec
+        per_lin_args[name], per_lin_N[name], per_flops[name] = (c, sc, t, A, B), N, fl
+        if name == "q_proj":
+            per_lin_N["K_qkv"] = K
     if want("a4"):
+        # q|k|v as one grouped call (they read the same x)
+        gq = [per_lin_args[n] for n in ("q_proj", "k_proj", "v_proj")]
+        yq = [torch.empty(M, Nq, dtype=torch.bfloat16, device=dev) for Nq in (per_lin_N[n] for n in ("q_proj", "k_proj", "v_proj"))]
+        wsg = torch.empty(q.grouped_ws_bytes(M, per_lin_N["K_qkv"], wl.r,
+                                             [per_lin_N[n] for n in ("q_proj", "k_proj", "v_proj")]),
+                          dtype=torch.uint8, device=dev)
+        xq = x[:, :per_lin_N["K_qkv"]].contiguous()
+        sec_g = timed(lambda: q.qerl_nvfp4_lora_linear_fwd_grouped(xq, gq, 2.0, packed=True, ys=yq, ws=wsg), 10)
+        fl_g = sum(per_flops[n] for n in ("q_proj", "k_proj", "v_proj"))
+        per["qkv_grouped"] = {"us": round(sec_g * 1e6, 1), "TFLOPs": round(fl_g / sec_g / 1e12, 1)}
+        lay_s = sec_g + sum(per[n]["us"] for n in ("o_proj", "gate_proj", "up_proj", "down_proj")) / 1e6
         rows["a4_prefill"] = {"workload": wl.name, "TFLOPs": round(tot_f / tot_s / 1e12, 1),
                               "frac_of_bf16_peak": round(tot_f / tot_s / 1e12 / bf16, 3),
+                              "layer_with_grouped_qkv_TFLOPs": round(tot_f / lay_s / 1e12, 1),
+                              "layer_with_grouped_qkv_frac": round(tot_f / lay_s / 1e12 / bf16, 3),
                               "peak": f"{kind} bf16_tflops {bf16}", "per_linear": per}
     if not want("a5"):
         torch.cuda.synchronize()

@@ -226,9 +226,9 @@ qerl_status qerl_nvfp4_unpack_codes(const uint8_t *packed, int64_t N, int64_t K,
  * Grouped forward: several linears that read the same x (in a decoder layer,
  * q|k|v and gate|up read one normalised input) in one call; the same result as
  * qerl_nvfp4_lora_linear_fwd (or _packed) on each group.  The pages have no
- * such call: it is an interface of this library that saves launches.  For
- * decode batches (M <= 64) the tensor-core path serves up to 3 groups in one
- * launch; other shapes run the groups one after the other.
+ * such call: it is an interface of this library that saves launches.  The
+ * tensor-core path serves up to 3 groups in one launch; more groups, or shapes
+ * it does not cover, run the groups one after the other.
  *   groups (host) [n_groups], 1 <= n_groups <= 8: per group N, codes, scales,
  *   tensor_scale, A [r, K], B [N, r], y [M, N] out, t_out optional [M, r].
  *   x (device) bf16 [M, K]; r, lora_scale and packed (0: standard codes,

@@ -802,7 +802,8 @@ FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r)
     pl.off_part = pl.u_bytes * G;
     pl.off_rows = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
     // many tokens: the down-projection runs as a split-K rows x rank product
-    pl.total = pl.off_rows + (G == 1 && M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r) : 0);
+    // (one buffer: the groups' down-projections run one after the other)
+    pl.total = pl.off_rows + (M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r) : 0);
     return pl;
 }
 
@@ -963,7 +964,6 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
         any_t = any_t || ga[g].t_out;
     }
     const FwdPlan pl = plan_fwd(a.M, Ns, G, a.K, a.r);
-    if (G > 1 && a.M > 64) return QERL_ERR_SHAPE;  // grouping serves decode tiles
     if (ws_bytes < pl.total) return QERL_ERR_WORKSPACE;
     float *partial = reinterpret_cast<float *>(ws + pl.off_part);
     const int tiles = pl.n_tiles * pl.m_tiles;

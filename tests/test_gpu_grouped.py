@@ -1,6 +1,7 @@
 """Grouped forward (linears sharing x) against the oracle, group by group: the
-one-launch tensor-core path (fused and unfused down-projection, packed and
-standard codes, ragged N) and the one-after-the-other fallback."""
+one-launch tensor-core path (fused and unfused down-projection, decode and
+many-token tiles, packed and standard codes, ragged N) and the
+one-after-the-other fallback."""
 import numpy as np
 import pytest
 import torch
@@ -61,9 +62,10 @@ def test_grouped_with_t_outputs():
     _check(cases, x, ys, t_outs=t_outs)
 
 
-@pytest.mark.parametrize("M,Ns", [(100, [256, 128]), (8, [128, 128, 128, 256])])
-def test_grouped_fallback_one_after_the_other(M, Ns):
-    """More than 64 tokens, or more than three groups: each group runs alone."""
+@pytest.mark.parametrize("M,Ns", [(100, [256, 128]), (300, [136, 256, 64]), (8, [128, 128, 128, 256])])
+def test_grouped_many_tokens_and_many_groups(M, Ns):
+    """More than 64 tokens: one launch, each group's down-projection on its own;
+    more than three groups: the groups run one after the other."""
     K, r = 512, 8
     cases, x, gs = _groups(M, K, Ns, r, False, seed=5)
     for c in cases:
