@@ -32,6 +32,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <numeric>
 #include <utility>
 
 #include "linear.cuh"
@@ -802,8 +803,8 @@ FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r)
     pl.off_part = pl.u_bytes * G;
     pl.off_rows = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
     // many tokens: the down-projection runs as a split-K rows x rank product
-    // (one buffer: the groups' down-projections run one after the other)
-    pl.total = pl.off_rows + (M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r) : 0);
+    // (one pass over x for every group)
+    pl.total = pl.off_rows + (M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r, G) : 0);
     return pl;
 }
 
@@ -838,10 +839,13 @@ const Env &env()
     return e;
 }
 
-// Largest cluster size in {4, 2, 1} that divides the weight tiles and still lets
-// the whole grid be resident at once (clusters are placed within one GPC).
+// Largest cluster size in {4, 2, 1} that divides every group's weight tiles
+// (`tile_unit` = the gcd of the groups' tile counts: the CTAs of a cluster share
+// one multicast of the token tiles, u included, so they must belong to one
+// linear) and still lets the whole grid be resident at once (clusters are
+// placed within one GPC).
 template <bool MULTICAST, typename Kernel>
-int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int n_tiles, unsigned grid)
+int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int tile_unit, unsigned grid)
 {
     static std::mutex mu;
     static std::map<std::pair<const void *, int>, int> max_clusters;  // (kernel, cs) -> resident clusters
@@ -849,7 +853,7 @@ int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int n_tiles, unsigned gr
     if (!forced && !MULTICAST) return 1;
     for (int cs = 4; cs >= 2; cs /= 2) {
         if (forced && cs != forced) continue;
-        if (n_tiles % cs != 0) continue;
+        if (tile_unit % cs != 0) continue;
         int dev = 0;
         cudaGetDevice(&dev);
         const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), cs * 64 + dev);
@@ -895,7 +899,9 @@ qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid,
     TcFwdParams p = p0;
     // Decode-sized token tiles are cheap to load per CTA, and clusters would tie
     // the CTAs' pipelines together; wide (prefill) tiles share them.
-    p.cs = pick_cluster<(BN >= 256)>(kernel, cfg, p.n_tiles, grid);
+    int unit = 0;
+    for (int g = 0; g < p.grp.G; ++g) unit = std::gcd(unit, p.grp.tile_start[g + 1] - p.grp.tile_start[g]);
+    p.cs = pick_cluster<(BN >= 256)>(kernel, cfg, unit, grid);
     // Programmatic dependent launch: the CTAs may start while the preceding
     // grid still runs and stream their (frozen) weights; the token producer and
     // the epilogue wait for that grid with griddepcontrol.wait.  Clusters of
@@ -999,13 +1005,19 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     //    the main kernel may then stream and dequantize its (frozen) weight
     //    while that work is still running.
     const bool chain = g_chain.load() != 0;
-    for (int g = 0; g < G && !fused; ++g) {
+    const bool rows = !fused && a.M > 64 && lora_down_rows_applies(a.K, a.r);
+    if (rows) {
+        DownRowsGroup dg[MAX_GROUPS];
+        for (int g = 0; g < G; ++g)
+            dg[g] = DownRowsGroup{ga[g].A, ga[g].tensor_scale, ga[g].t_out,
+                                  reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u + g * pl.u_bytes)};
+        QERL_TRY(lora_down_rows(a.x, a.M, a.K, dg, G, a.r, pl.r_pad, a.lora_scale,
+                                reinterpret_cast<float *>(ws + pl.off_rows), chain, s));
+    }
+    for (int g = 0; g < G && !fused && !rows; ++g) {
         const FwdArgs &b = ga[g];
         __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u + g * pl.u_bytes);
-        if (a.M > 64 && lora_down_rows_applies(a.K, a.r)) {
-            QERL_TRY(lora_down_rows(a.x, a.M, a.K, b.A, a.r, pl.r_pad, a.lora_scale, b.tensor_scale, b.t_out, u,
-                                    reinterpret_cast<float *>(ws + pl.off_rows), chain, s));
-        } else if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
+        if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
             constexpr int MB = 4, JB = 2;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
             QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,

@@ -62,10 +62,15 @@ def test_grouped_with_t_outputs():
     _check(cases, x, ys, t_outs=t_outs)
 
 
-@pytest.mark.parametrize("M,Ns", [(100, [256, 128]), (300, [136, 256, 64]), (8, [128, 128, 128, 256])])
+@pytest.mark.parametrize("M,Ns", [(100, [256, 128]), (300, [136, 256, 64]), (8, [128, 128, 128, 256]),
+                                  (200, [128, 256, 64]), (1000, [256, 128, 128]), (256, [256, 256]),
+                                  (512, [512, 128, 128])])
 def test_grouped_many_tokens_and_many_groups(M, Ns):
-    """More than 64 tokens: one launch, each group's down-projection on its own;
-    more than three groups: the groups run one after the other."""
+    """More than 64 tokens: one launch, one down-projection pass for all groups;
+    more than three groups: the groups run one after the other.  With 256-token
+    tiles the CTAs may form clusters that share the token tiles: a cluster never
+    spans two groups (4 weight tiles in all, split 1 + 2 + 1, must not cluster),
+    and groups whose tile counts allow it still cluster inside each group."""
     K, r = 512, 8
     cases, x, gs = _groups(M, K, Ns, r, False, seed=5)
     for c in cases:
