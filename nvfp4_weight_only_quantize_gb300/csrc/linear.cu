@@ -597,16 +597,25 @@ size_t thin_wide_ws(int64_t M, int64_t Wd, int r)
     return round256(size_t(thin_splits((Wd + tr - 1) / tr, M)) * Wd * r * sizeof(float));
 }
 
-// t = sum of the split partials (fixed order); t_out = t (optional); u =
-// bf16(s t / (s_t 2^c)) as [M, r_pad], zeros past r: the LoRA operand of the
-// tensor-core forward.
-__global__ void __launch_bounds__(256) u_reduce_kernel(const float *__restrict__ part, int splits, int64_t M, int r,
-                                                       int r_pad, float s, const float *__restrict__ tensor_scale,
-                                                       float *__restrict__ t_out, __nv_bfloat16 *__restrict__ u)
+// Per group g (blockIdx.y): t = sum of the split partials (fixed order);
+// t_out = t (optional); u = bf16(s t / (s_t 2^c)) as [M, r_pad], zeros past
+// r: the LoRA operand of the tensor-core forward.
+struct UReduceGroups {
+    const float *part[RANK_MAX_G];
+    const float *tensor_scale[RANK_MAX_G];
+    float *t_out[RANK_MAX_G];
+    __nv_bfloat16 *u[RANK_MAX_G];
+};
+__global__ void __launch_bounds__(256) u_reduce_kernel(const UReduceGroups grp, int splits, int64_t M, int r,
+                                                       int r_pad, float s)
 {
     pdl_trigger();
     pdl_wait();
-    const float st = *tensor_scale;
+    const int g = blockIdx.y;
+    const float *part = grp.part[g];
+    float *t_out = grp.t_out[g];
+    __nv_bfloat16 *u = grp.u[g];
+    const float st = *grp.tensor_scale[g];
     const float fac = s / (st * pow2f(tc_exponent_offset(st)));
     const int64_t n = M * r_pad;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -621,16 +630,39 @@ __global__ void __launch_bounds__(256) u_reduce_kernel(const float *__restrict__
     }
 }
 
+// B [N, r] -> B^T [r, N] (the rank-side operand of v = dy B on tensor cores).
+__global__ void __launch_bounds__(256) transpose_rank_kernel(const __nv_bfloat16 *__restrict__ B, int64_t N, int r,
+                                                             __nv_bfloat16 *__restrict__ bt)
+{
+    for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N; n += (int64_t)gridDim.x * blockDim.x)
+        for (int j = 0; j < r; ++j) bt[(int64_t)j * N + n] = B[n * r + j];
+}
+
+// out = alpha * X W^T (+ out if accumulate) with W [r, Kd]: the tensor-core
+// rank product, then the split reduction.
+qerl_status rank_rows(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const __nv_bfloat16 *W, int r, StoreF32 ep,
+                      float *part, cudaStream_t s)
+{
+    const RankOut o{W, r, part};
+    QERL_TRY(rank_tc(X, M, Kd, &o, 1, g_chain.load() != 0, s));
+    int64_t g = (M * r + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    split_reduce<<<(unsigned)g, 256, 0, s>>>(part, rank_tc_splits(M, Kd), M, r, ep.out, ep.ld, ep.alpha,
+                                             ep.accumulate);
+    return launched();
+}
+
 // Scratch of the backward: v, t (when not saved), v' for the tensor-core dx,
 // and the split-k partials of the thin products.
 struct BwdWs {
-    size_t vbytes, vp_bytes, part_bytes;
+    size_t vbytes, vp_bytes, bt_bytes, part_bytes;
 };
 BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
 {
     BwdWs w;
     w.vbytes = round256(size_t(M) * r * sizeof(float));
     w.vp_bytes = tc_dx_ws_bytes(M, r);
+    w.bt_bytes = r <= 64 ? round256(size_t(r) * N * 2) : 0;
     size_t pb = gemm_split_ws(M, r, N);                               // v = dy B
     pb = std::max(pb, gemm_split_ws(M, r, K));                         // t = x A^T
     pb = std::max(pb, gemm_split_ws(r, K, M));                         // dA
@@ -640,6 +672,8 @@ BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
         pb = std::max(pb, thin_rows_ws(M, K, r));
         pb = std::max(pb, thin_wide_ws(M, K, r));
         pb = std::max(pb, thin_wide_ws(M, N, r));
+        pb = std::max(pb, rank_tc_part_bytes(M, N, r));
+        pb = std::max(pb, rank_tc_part_bytes(M, K, r));
     }
     w.part_bytes = pb;
     return w;
@@ -654,12 +688,22 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     float *v = reinterpret_cast<float *>(ws);
     float *u = reinterpret_cast<float *>(ws + w.vbytes);
     char *vp = ws + 2 * w.vbytes;
-    float *part = reinterpret_cast<float *>(vp + w.vp_bytes);
+    __nv_bfloat16 *bt = reinterpret_cast<__nv_bfloat16 *>(vp + w.vp_bytes);
+    float *part = reinterpret_cast<float *>(vp + w.vp_bytes + w.bt_bytes);
     // the thin products take the dedicated kernels when every operand is a
     // whole number of 16-byte vectors
     const bool thin = thin_ok(a.N, a.r) && thin_ok(a.K, a.r) && aligned16(a.dy) && aligned16(a.x) &&
                       aligned16(a.A) && aligned16(a.B);
-    if (thin)
+    // the rows x rank products (v = dy B, t = x A^T) on tensor cores
+    const bool rank = thin && g_algo.load() != QERL_ALGO_SIMT && rank_tc_applies(a.M, a.N, a.r, a.dy, bt) &&
+                      rank_tc_applies(a.M, a.K, a.r, a.x, a.A);
+    if (rank) {
+        int64_t g = (a.N + 255) / 256;
+        if (g > 4 * num_sms()) g = 4 * num_sms();
+        transpose_rank_kernel<<<(unsigned)g, 256, 0, s>>>(a.B, a.N, a.r, bt);
+        QERL_TRY(launched());
+        QERL_TRY(rank_rows(a.dy, a.M, a.N, bt, a.r, StoreF32{v, a.r, 1.0f, 0}, part, s));
+    } else if (thin)
         QERL_TRY(thin_rows(a.dy, a.M, a.N, a.B, false, a.r, StoreF32{v, a.r, 1.0f, 0}, part, s));
     else
         QERL_TRY(run_gemm_store(a.M, a.r, a.N, RowBF16{a.dy, a.N}, ColBF16{a.B, a.r}, StoreF32{v, a.r, 1.0f, 0},
@@ -681,7 +725,9 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     if (a.dB) {
         const float *uu = a.t_saved;
         if (!uu) {
-            if (thin)
+            if (rank)
+                QERL_TRY(rank_rows(a.x, a.M, a.K, a.A, a.r, StoreF32{u, a.r, 1.0f, 0}, part, s));
+            else if (thin)
                 QERL_TRY(thin_rows(a.x, a.M, a.K, a.A, true, a.r, StoreF32{u, a.r, 1.0f, 0}, part, s));
             else
                 QERL_TRY(run_gemm_store(a.M, a.r, a.K, RowBF16{a.x, a.K}, RowBF16{a.A, a.K},
@@ -710,28 +756,62 @@ qerl_status check_common(int64_t M, int64_t K, int64_t N, const uint8_t *codes, 
 }  // namespace
 
 bool lora_down_rows_applies(int64_t K, int r) { return thin_ok(K, r); }
-size_t lora_down_rows_ws(int64_t M, int64_t K, int r) { return thin_rows_ws(M, K, r); }
-
-qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const __nv_bfloat16 *A, int r, int r_pad,
-                           float s, const float *tensor_scale, float *t_out, __nv_bfloat16 *u, float *part,
-                           bool chain, cudaStream_t st)
+size_t lora_down_rows_ws(int64_t M, int64_t K, int r, int G)
 {
+    return std::max(size_t(G) * rank_tc_part_bytes(M, K, r), thin_rows_ws(M, K, r));
+}
+
+qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const DownRowsGroup *grp, int G, int r,
+                           int r_pad, float s, float *part, bool chain, cudaStream_t st)
+{
+    if (G < 1 || G > RANK_MAX_G) return QERL_ERR_INVALID_ARG;
+    int64_t gred = (M * r_pad + 255) / 256;
+    if (gred > 8 * num_sms()) gred = 8 * num_sms();
+    UReduceGroups ug;
+    for (int g = 0; g < RANK_MAX_G; ++g) {
+        const DownRowsGroup &d = grp[g < G ? g : 0];
+        ug.part[g] = nullptr;
+        ug.tensor_scale[g] = d.tensor_scale;
+        ug.t_out[g] = d.t_out;
+        ug.u[g] = d.u;
+    }
+    bool tc = g_algo.load() != QERL_ALGO_SIMT;
+    for (int g = 0; g < G && tc; ++g) tc = rank_tc_applies(M, K, r, x, grp[g].A);
+    if (tc) {  // one pass over x for every group
+        const size_t pb = rank_tc_part_bytes(M, K, r);
+        RankOut outs[RANK_MAX_G];
+        for (int g = 0; g < G; ++g) {
+            outs[g] = RankOut{grp[g].A, r, reinterpret_cast<float *>(reinterpret_cast<char *>(part) + g * pb)};
+            ug.part[g] = outs[g].part;
+        }
+        QERL_TRY(rank_tc(x, M, K, outs, G, chain, st));
+        return launched(launch_k(u_reduce_kernel, dim3((unsigned)gred, (unsigned)G), dim3(256), 0, st, chain, ug,
+                                 rank_tc_splits(M, K), M, r, r_pad, s));
+    }
+    // CUDA cores, group by group through the same partials buffer
     const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
     const int64_t tiles = (M + tr - 1) / tr;
     const int sp = thin_splits(tiles, K);
     const int64_t kchunk = ((K + sp - 1) / sp + THIN_TK - 1) / THIN_TK * THIN_TK;
     const int splits = (int)((K + kchunk - 1) / kchunk);
     const dim3 grid((unsigned)tiles, (unsigned)splits);
-    if (r <= 32)
-        QERL_TRY(launched(launch_k(thin_rows_kernel<true, 32>, grid, dim3(256), 0, st, chain, x, M, K, A, r, kchunk,
-                                   part)));
-    else
-        QERL_TRY(launched(launch_k(thin_rows_kernel<true, 64>, grid, dim3(256), 0, st, chain, x, M, K, A, r, kchunk,
-                                   part)));
-    int64_t g = (M * r_pad + 255) / 256;
-    if (g > 8 * num_sms()) g = 8 * num_sms();
-    return launched(launch_k(u_reduce_kernel, dim3((unsigned)g), dim3(256), 0, st, chain, (const float *)part, splits,
-                             M, r, r_pad, s, tensor_scale, t_out, u));
+    for (int g = 0; g < G; ++g) {
+        const __nv_bfloat16 *A = grp[g].A;
+        if (r <= 32)
+            QERL_TRY(launched(launch_k(thin_rows_kernel<true, 32>, grid, dim3(256), 0, st, chain, x, M, K, A, r,
+                                       kchunk, part)));
+        else
+            QERL_TRY(launched(launch_k(thin_rows_kernel<true, 64>, grid, dim3(256), 0, st, chain, x, M, K, A, r,
+                                       kchunk, part)));
+        UReduceGroups one = ug;
+        one.part[0] = part;
+        one.tensor_scale[0] = grp[g].tensor_scale;
+        one.t_out[0] = grp[g].t_out;
+        one.u[0] = grp[g].u;
+        QERL_TRY(launched(launch_k(u_reduce_kernel, dim3((unsigned)gred, 1u), dim3(256), 0, st, chain, one, splits, M,
+                                   r, r_pad, s)));
+    }
+    return QERL_OK;
 }
 
 size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
@@ -744,7 +824,7 @@ size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {
     const BwdWs w = bwd_ws(M, N, K, r);
-    return 2 * w.vbytes + w.vp_bytes + w.part_bytes;
+    return 2 * w.vbytes + w.vp_bytes + w.bt_bytes + w.part_bytes;
 }
 
 qerl_status linear_fwd_fixed_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,

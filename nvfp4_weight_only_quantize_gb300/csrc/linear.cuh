@@ -54,14 +54,38 @@ inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
-// LoRA down-projection for many tokens (CUDA cores, split over K): t = x A^T,
-// t_out = t when given, u = bf16(s t / (s_t 2^c)) [M, r_pad] (zeros past r);
-// part holds lora_down_rows_ws(M, K, r) bytes.  Chained launches when `chain`.
+// Rank products on tensor cores (rank_tc.cu), split over the reduction: for g < G,
+//   part_g[z][m][j] = sum over k in split z of X[m, k] * W_g[j, k],  j < r_g,
+// X [M, Kd] and W_g [r_g, Kd] bf16 row-major, 16-byte aligned, Kd % 8 == 0,
+// Kd >= 64, r_g <= 64; part_g holds rank_tc_part_bytes(M, Kd, r_g) bytes, and the
+// rank_tc_splits(M, Kd) partials are summed in split order by the caller.
+constexpr int RANK_MAX_G = 3;
+struct RankOut {
+    const __nv_bfloat16 *W;
+    int r;
+    float *part;
+};
+bool rank_tc_applies(int64_t M, int64_t Kd, int r, const void *X, const void *W);
+int rank_tc_splits(int64_t M, int64_t Kd);
+size_t rank_tc_part_bytes(int64_t M, int64_t Kd, int r);
+qerl_status rank_tc(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const RankOut *outs, int G, bool chain,
+                    cudaStream_t s);
+
+// LoRA down-projection for many tokens, for G (<= 3) linears sharing x (one
+// pass over x on tensor cores where rank_tc applies, else CUDA cores group by
+// group): t_g = x A_g^T, t_out_g = t_g when given, u_g = bf16(s t_g / (s_t,g
+// 2^c_g)) [M, r_pad] (zeros past r).  part holds lora_down_rows_ws(M, K, r, G)
+// bytes.  Chained launches when `chain`.
+struct DownRowsGroup {
+    const __nv_bfloat16 *A;
+    const float *tensor_scale;
+    float *t_out;
+    __nv_bfloat16 *u;
+};
 bool lora_down_rows_applies(int64_t K, int r);
-size_t lora_down_rows_ws(int64_t M, int64_t K, int r);
-qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const __nv_bfloat16 *A, int r, int r_pad,
-                           float s, const float *tensor_scale, float *t_out, __nv_bfloat16 *u, float *part,
-                           bool chain, cudaStream_t st);
+size_t lora_down_rows_ws(int64_t M, int64_t K, int r, int G);
+qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const DownRowsGroup *grp, int G, int r,
+                           int r_pad, float s, float *part, bool chain, cudaStream_t st);
 
 // Tensor-core input gradient dx = dy w_hat + s v A for the shapes it covers
 // (K % 256 == 0, N % 64 == 0, r <= 256); v = dy B in FP32 [M, r] is given, and
