@@ -478,8 +478,8 @@ def other_rows(dev, only=None, profile=False):
     rows["a5_backward"] = {"workload": f"qwen2.5-7b {name} {N}x{K}, M={M}, r={wl.r}", "us": round(sec * 1e6, 1),
                            "TFLOPs": round(fl / sec / 1e12, 2),
                            "frac_of_bf16_peak": round(fl / sec / 1e12 / bf16, 3),
-                           "path": "dx, v = dy B and t = x A^T on tensor cores (tcgen05; dx with transposed "
-                                   "dequant, v and t as split-K rank products); dA, dB on CUDA cores"}
+                           "path": "every product on tensor cores (tcgen05): dx with transposed dequant; v = dy B, "
+                                   "t = x A^T, dA = s v^T x, dB = s dy^T t as split-K rank products"}
     torch.cuda.synchronize()
     return rows
 

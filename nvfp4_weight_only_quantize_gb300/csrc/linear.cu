@@ -630,6 +630,20 @@ __global__ void __launch_bounds__(256) u_reduce_kernel(const UReduceGroups grp, 
     }
 }
 
+// out = alpha * P (+ out if accumulate), P[w][j] (wj) or P[j][w] = sum over m
+// of D[m, w] T[m, j]: the tensor-core wide product, then the split reduction.
+qerl_status wide_rows(const __nv_bfloat16 *D, int64_t M, int64_t Wd, const float *T, int r, bool wj, StoreF32 ep,
+                      __nv_bfloat16 *tb, float *part, cudaStream_t s)
+{
+    QERL_TRY(wide_tc(D, M, Wd, T, r, wj, tb, part, g_chain.load() != 0, s));
+    const int64_t P = wj ? Wd : r, Q = wj ? r : Wd;
+    int64_t g = (P * Q + 255) / 256;
+    if (g > 8 * num_sms()) g = 8 * num_sms();
+    split_reduce<<<(unsigned)g, 256, 0, s>>>(part, wide_tc_splits(M, Wd), P, Q, ep.out, ep.ld, ep.alpha,
+                                             ep.accumulate);
+    return launched();
+}
+
 // B [N, r] -> B^T [r, N] (the rank-side operand of v = dy B on tensor cores).
 __global__ void __launch_bounds__(256) transpose_rank_kernel(const __nv_bfloat16 *__restrict__ B, int64_t N, int r,
                                                              __nv_bfloat16 *__restrict__ bt)
@@ -655,7 +669,7 @@ qerl_status rank_rows(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const __nv_
 // Scratch of the backward: v, t (when not saved), v' for the tensor-core dx,
 // and the split-k partials of the thin products.
 struct BwdWs {
-    size_t vbytes, vp_bytes, bt_bytes, part_bytes;
+    size_t vbytes, vp_bytes, bt_bytes, tb_bytes, part_bytes;
 };
 BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
 {
@@ -663,6 +677,7 @@ BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
     w.vbytes = round256(size_t(M) * r * sizeof(float));
     w.vp_bytes = tc_dx_ws_bytes(M, r);
     w.bt_bytes = r <= 64 ? round256(size_t(r) * N * 2) : 0;
+    w.tb_bytes = r <= 64 ? wide_tc_tb_bytes(M, r) : 0;
     size_t pb = gemm_split_ws(M, r, N);                               // v = dy B
     pb = std::max(pb, gemm_split_ws(M, r, K));                         // t = x A^T
     pb = std::max(pb, gemm_split_ws(r, K, M));                         // dA
@@ -674,6 +689,8 @@ BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
         pb = std::max(pb, thin_wide_ws(M, N, r));
         pb = std::max(pb, rank_tc_part_bytes(M, N, r));
         pb = std::max(pb, rank_tc_part_bytes(M, K, r));
+        pb = std::max(pb, wide_tc_part_bytes(M, K, r));
+        pb = std::max(pb, wide_tc_part_bytes(M, N, r));
     }
     w.part_bytes = pb;
     return w;
@@ -689,7 +706,8 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     float *u = reinterpret_cast<float *>(ws + w.vbytes);
     char *vp = ws + 2 * w.vbytes;
     __nv_bfloat16 *bt = reinterpret_cast<__nv_bfloat16 *>(vp + w.vp_bytes);
-    float *part = reinterpret_cast<float *>(vp + w.vp_bytes + w.bt_bytes);
+    __nv_bfloat16 *tb = reinterpret_cast<__nv_bfloat16 *>(vp + w.vp_bytes + w.bt_bytes);
+    float *part = reinterpret_cast<float *>(vp + w.vp_bytes + w.bt_bytes + w.tb_bytes);
     // the thin products take the dedicated kernels when every operand is a
     // whole number of 16-byte vectors
     const bool thin = thin_ok(a.N, a.r) && thin_ok(a.K, a.r) && aligned16(a.dy) && aligned16(a.x) &&
@@ -697,6 +715,9 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     // the rows x rank products (v = dy B, t = x A^T) on tensor cores
     const bool rank = thin && g_algo.load() != QERL_ALGO_SIMT && rank_tc_applies(a.M, a.N, a.r, a.dy, bt) &&
                       rank_tc_applies(a.M, a.K, a.r, a.x, a.A);
+    // the wide x rank products (dA, dB) on tensor cores
+    const bool wide = thin && g_algo.load() != QERL_ALGO_SIMT && wide_tc_applies(a.M, a.K, a.r, a.x) &&
+                      wide_tc_applies(a.M, a.N, a.r, a.dy);
     if (rank) {
         int64_t g = (a.N + 255) / 256;
         if (g > 4 * num_sms()) g = 4 * num_sms();
@@ -717,7 +738,9 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     }
     if (a.dA) {
         const StoreF32 ep{a.dA, a.K, a.lora_scale, a.accumulate};
-        if (thin)
+        if (wide)
+            QERL_TRY(wide_rows(a.x, a.M, a.K, v, a.r, false, ep, tb, part, s));
+        else if (thin)
             QERL_TRY(thin_wide(a.x, a.M, a.K, v, a.r, false, ep, part, s));
         else
             QERL_TRY(run_gemm_store((int64_t)a.r, a.K, a.M, ColF32{v, a.r}, ColBF16{a.x, a.K}, ep, part, s));
@@ -735,7 +758,9 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
             uu = u;
         }
         const StoreF32 ep{a.dB, a.r, a.lora_scale, a.accumulate};
-        if (thin)
+        if (wide)
+            QERL_TRY(wide_rows(a.dy, a.M, a.N, uu, a.r, true, ep, tb, part, s));
+        else if (thin)
             QERL_TRY(thin_wide(a.dy, a.M, a.N, uu, a.r, true, ep, part, s));
         else
             QERL_TRY(run_gemm_store(a.N, (int64_t)a.r, a.M, ColBF16{a.dy, a.N}, ColF32{uu, a.r}, ep, part, s));
@@ -824,7 +849,7 @@ size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {
     const BwdWs w = bwd_ws(M, N, K, r);
-    return 2 * w.vbytes + w.vp_bytes + w.bt_bytes + w.part_bytes;
+    return 2 * w.vbytes + w.vp_bytes + w.bt_bytes + w.tb_bytes + w.part_bytes;
 }
 
 qerl_status linear_fwd_fixed_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,

@@ -71,6 +71,19 @@ size_t rank_tc_part_bytes(int64_t M, int64_t Kd, int r);
 qerl_status rank_tc(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const RankOut *outs, int G, bool chain,
                     cudaStream_t s);
 
+// Wide x rank products on tensor cores (rank_tc.cu), split over the tokens:
+//   part[z][w][j] (wj) or part[z][j][w] = sum over m in split z of D[m, w] * T[m, j],
+// D bf16 [M, Wd] row-major, 16-byte aligned, Wd % 8 == 0, Wd >= 64; T FP32
+// [M, r], r <= 64.  tb holds wide_tc_tb_bytes(M, r) bytes of scratch (T as a
+// bf16 hi/lo pair), part wide_tc_part_bytes(M, Wd, r); the wide_tc_splits(M, Wd)
+// partials are summed in split order by the caller.
+bool wide_tc_applies(int64_t M, int64_t Wd, int r, const void *D);
+int wide_tc_splits(int64_t M, int64_t Wd);
+size_t wide_tc_part_bytes(int64_t M, int64_t Wd, int r);
+size_t wide_tc_tb_bytes(int64_t M, int r);
+qerl_status wide_tc(const __nv_bfloat16 *D, int64_t M, int64_t Wd, const float *T, int r, bool wj,
+                    __nv_bfloat16 *tb, float *part, bool chain, cudaStream_t s);
+
 // LoRA down-projection for many tokens, for G (<= 3) linears sharing x (one
 // pass over x on tensor cores where rank_tc applies, else CUDA cores group by
 // group): t_g = x A_g^T, t_out_g = t_g when given, u_g = bf16(s t_g / (s_t,g

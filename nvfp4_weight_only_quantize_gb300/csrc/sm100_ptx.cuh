@@ -227,11 +227,27 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr)
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// As above for an MN-major operand in the 128-byte swizzled canonical layout:
+// each K row holds 64 consecutive MN elements (128 B), 8 K rows form one
+// 1024-byte swizzle atom; `lbo` = byte distance between 64-element MN blocks,
+// `sbo` = byte distance between 8-row K groups.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor, kind::f16: D f32 (bit 4), A bf16 (bits 7-9 = 1),
 // B bf16 (bits 10-12 = 1), both K-major, N>>3 at bit 17, M>>4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// As above with A and B both MN-major (the transpose bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N)
+{
+    return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
 }
 
 // ------------------------------------------------------------------ misc

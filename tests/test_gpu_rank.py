@@ -50,11 +50,13 @@ def test_backward_rank_products(M, K, N, r):
 
 
 def test_backward_rank_matches_cuda_cores():
-    """The tensor-core and CUDA-core rank products give the same gradients up to
-    FP32 summation order: dA = s v^T x and dB = s dy^T t (FP32, both fed by the
-    rank products) to 1e-5.  dx is only held to the oracle tolerance here: the
-    tensor-core dx takes its LoRA term through a bf16 copy of v, the CUDA-core
-    dx through the FP32 v."""
+    """The tensor-core and CUDA-core rank products give the same weight
+    gradients dA = s v^T x and dB = s dy^T t to 5e-5: the tensor-core wide
+    products take the FP32 v and t as a bf16 pair hi + lo, exact to 2^-18
+    relative per term, so over ~25k outputs the worst one strays about
+    4 x 2^-18 = 1.5e-5 of the rms, plus the FP32 summation order.  dx is only
+    held to the oracle tolerance here: the tensor-core dx takes its LoRA term
+    through a bf16 copy of v, the CUDA-core dx through the FP32 v."""
     c = LinearCase(515, 1024, 320, 24, config=9, idx=11).quantize_gpu()
     outs = {}
     try:
@@ -67,7 +69,7 @@ def test_backward_rank_matches_cuda_cores():
         q.set_linear_algo(q.ALGO_AUTO)
     assert_rel_rms(f64(outs[q.ALGO_AUTO][0]), f64(outs[q.ALGO_SIMT][0]), LIN_TOL, "dx")
     for name, a, b in zip(("dA", "dB"), outs[q.ALGO_AUTO][1:], outs[q.ALGO_SIMT][1:]):
-        assert_rel_rms(f64(a), f64(b), 1e-5, name)
+        assert_rel_rms(f64(a), f64(b), 5e-5, name)
 
 
 @pytest.mark.parametrize("M,Ns,r", [(200, [128, 256, 64], 12), (130, [136, 72], 40), (1000, [256, 128, 128], 32)])
