@@ -370,6 +370,69 @@ def _time_fn(fn, reps, warm=3):
     return e0.elapsed_time(e1) / 1e3 / reps
 
 
+SWEEP_RANKS = (8, 16, 32, 64, 128)
+
+
+def rank_sweep(dev):
+    """LoRA-rank sweep of the forward, and the same linear with 16-bit weights.
+    Decode: Qwen2.5-7B gate_proj 18944 x 3584 at M = 64, four weight copies
+    rotated in one CUDA graph (152 MB NVFP4, 543 MB bf16: both above L2).
+    Prefill: Qwen2.5-14B q_proj 5120 x 5120 at M = 4096.  The 16-bit arm is
+    y = x W^T + s (x A^T) B^T in torch (cuBLAS) with W the dequantized weight of
+    the same codes rounded to bf16, so both arms compute the same product."""
+    import nvfp4_weight_only_quantize_gb300 as q
+    from nvfp4_weight_only_quantize_gb300 import synth
+    out = {}
+    for tag, (N, K, M, n_copies) in (("decode", (18944, 3584, 64, 4)), ("prefill", (5120, 5120, 4096, 1))):
+        x = synth.activations(M, K, 70, dev)
+        qw, w16 = [], []
+        for c in range(n_copies):
+            W = synth.weight(N, K, 71 + c, dev)
+            codes, sc, ts = q.qerl_nvfp4_quantize(W)
+            w16.append(q.qerl_nvfp4_dequantize(codes, sc, ts, N, K))  # bf16, tensor scale applied
+            del W
+            q.qerl_nvfp4_pack_codes(codes, out=codes)
+            qw.append((codes, sc, ts))
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        res = {}
+        for r in SWEEP_RANKS:
+            lora = [(synth.lora_A(r, K, 80 + c, dev), synth.lora_B(N, r, 90 + c, dev)) for c in range(n_copies)]
+            ws = q.workspace(q.OP_LINEAR_FWD, M, N, K, r, dev)
+
+            def ours():
+                for (codes, sc, ts), (A, B) in zip(qw, lora):
+                    q.qerl_nvfp4_lora_linear_fwd_packed(x, codes, sc, ts, A, B, 2.0, y=y, ws=ws)
+
+            def bf16():
+                for W16, (A, B) in zip(w16, lora):
+                    torch.mm(x, W16.t(), out=y)
+                    y.add_(torch.mm(torch.mm(x, A.t()), B.t()), alpha=2.0)
+
+            reps = 20 if tag == "decode" else 5
+            us = {}
+            for arm, fn in (("nvfp4", ours), ("bf16", bf16)):
+                g = _graph(fn)
+                _time_graph(g, 3)
+                us[arm] = _time_graph(g, reps) / (reps * n_copies) * 1e6
+                del g
+            fl = 2.0 * M * N * K + 2.0 * M * r * (N + K)
+            if tag == "decode":
+                res[r] = {"us": round(us["nvfp4"], 2), "GBps": round(linear_bytes(N, K, r) / us["nvfp4"] / 1e3, 1),
+                          "bf16_us": round(us["bf16"], 2),
+                          "bf16_GBps": round((2.0 * N * K + 2 * r * (N + K)) / us["bf16"] / 1e3, 1),
+                          "speedup_vs_bf16": round(us["bf16"] / us["nvfp4"], 3)}
+            else:
+                res[r] = {"us": round(us["nvfp4"], 1), "TFLOPs": round(fl / us["nvfp4"] / 1e6, 1),
+                          "bf16_us": round(us["bf16"], 1), "bf16_TFLOPs": round(fl / us["bf16"] / 1e6, 1),
+                          "speedup_vs_bf16": round(us["bf16"] / us["nvfp4"], 3)}
+        out[tag] = {"workload": (f"qwen2.5-7b gate_proj {N}x{K}, M={M}, {n_copies} rotated weight copies"
+                                 if tag == "decode" else f"qwen2.5-14b q_proj {N}x{K}, M={M}"),
+                    "by_rank": res}
+        del qw, w16, x, y
+        torch.cuda.synchronize()
+    return out
+
+
 def other_rows(dev, only=None, profile=False):
     """Each remaining hot-path row on its own workload (CUDA events, after warm-up):
     the quantizer on a Qwen2.5-7B gate_proj weight, AQN-RMSNorm at decode and
@@ -454,6 +517,8 @@ def other_rows(dev, only=None, profile=False):
                               "layer_with_grouped_qkv_TFLOPs": round(tot_f / lay_s / 1e12, 1),
                               "layer_with_grouped_qkv_frac": round(tot_f / lay_s / 1e12 / bf16, 3),
                               "peak": f"{kind} bf16_tflops {bf16}", "per_linear": per}
+    if want("f2"):
+        rows["f2_lora_rank_sweep"] = rank_sweep(dev)
     if not want("a5"):
         torch.cuda.synchronize()
         return rows
@@ -557,7 +622,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize/norm/prefill/backward lines")
-    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5"],
+    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5", "f2"],
                     help="run only that row's measurement, its timed launches bracketed by "
                          "cudaProfilerStart/Stop (for ncu --profile-from-start off), and print it")
     ap.add_argument("--codes", default="packed", choices=["packed", "standard"],

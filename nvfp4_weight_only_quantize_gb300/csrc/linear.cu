@@ -780,10 +780,11 @@ qerl_status check_common(int64_t M, int64_t K, int64_t N, const uint8_t *codes, 
 
 }  // namespace
 
-bool lora_down_rows_applies(int64_t K, int r) { return thin_ok(K, r); }
+// r <= 64: tensor cores or the CUDA-core fallback; 64 < r <= 128: tensor cores only
+bool lora_down_rows_applies(int64_t K, int r) { return thin_ok(K, r) || (r <= 128 && K % 8 == 0 && K >= 64); }
 size_t lora_down_rows_ws(int64_t M, int64_t K, int r, int G)
 {
-    return std::max(size_t(G) * rank_tc_part_bytes(M, K, r), thin_rows_ws(M, K, r));
+    return std::max(size_t(G) * rank_tc_part_bytes(M, K, r), r <= 64 ? thin_rows_ws(M, K, r) : size_t(0));
 }
 
 qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const DownRowsGroup *grp, int G, int r,
@@ -809,10 +810,14 @@ qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const D
             outs[g] = RankOut{grp[g].A, r, reinterpret_cast<float *>(reinterpret_cast<char *>(part) + g * pb)};
             ug.part[g] = outs[g].part;
         }
-        QERL_TRY(rank_tc(x, M, K, outs, G, chain, st));
+        // groups per launch: their padded ranks fit the MMA's 256 columns
+        const int per = std::min(G, 256 / rank_tc_pad(r));
+        for (int g0 = 0; g0 < G; g0 += per)
+            QERL_TRY(rank_tc(x, M, K, outs + g0, std::min(per, G - g0), chain, st));
         return launched(launch_k(u_reduce_kernel, dim3((unsigned)gred, (unsigned)G), dim3(256), 0, st, chain, ug,
                                  rank_tc_splits(M, K), M, r, r_pad, s));
     }
+    if (r > 64) return QERL_ERR_SHAPE;  // the CUDA-core kernel covers r <= 64
     // CUDA cores, group by group through the same partials buffer
     const int tr = r <= 32 ? thin_tr<32>() : thin_tr<64>();
     const int64_t tiles = (M + tr - 1) / tr;

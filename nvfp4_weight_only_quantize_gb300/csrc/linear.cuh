@@ -57,9 +57,11 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
 // Rank products on tensor cores (rank_tc.cu), split over the reduction: for g < G,
 //   part_g[z][m][j] = sum over k in split z of X[m, k] * W_g[j, k],  j < r_g,
 // X [M, Kd] and W_g [r_g, Kd] bf16 row-major, 16-byte aligned, Kd % 8 == 0,
-// Kd >= 64, r_g <= 64; part_g holds rank_tc_part_bytes(M, Kd, r_g) bytes, and the
-// rank_tc_splits(M, Kd) partials are summed in split order by the caller.
+// Kd >= 64, r_g <= 128, and G * rank_tc_pad(max r_g) <= 256 (else QERL_ERR_SHAPE);
+// part_g holds rank_tc_part_bytes(M, Kd, r_g) bytes, and the rank_tc_splits(M, Kd)
+// partials are summed in split order by the caller.
 constexpr int RANK_MAX_G = 3;
+inline int rank_tc_pad(int r) { return r <= 32 ? 32 : r <= 64 ? 64 : 128; }
 struct RankOut {
     const __nv_bfloat16 *W;
     int r;

@@ -7,8 +7,8 @@
 // bf16 [r_g, Kd] row-major (A, or B^T); P_g FP32 [splits][M][r_g]: the split
 // partials, summed in split order by the caller's reduction kernel.
 //
-// One CTA: 128 tokens (MMA M) x G * RP ranks (MMA N; rows r_g .. RP-1 of each
-// group are the TMA zero fill) over one split of the reduction, 64 k per stage
+// One CTA: 128 tokens (MMA M) x G * RP ranks (MMA N <= 256, RP = 32, 64 or 128;
+// rows r_g .. RP-1 of each group are the TMA zero fill) over one split of the reduction, 64 k per stage
 // (one X box of 128 x 64 and one RP x 64 box per group, K-major, 128-byte
 // swizzle).  The accumulator sits in TMEM, lane = token.  Warp 0 issues the TMA
 // loads, warp 1 owns TMEM and issues the MMAs, all four warps run the epilogue.
@@ -463,7 +463,7 @@ struct RankPlan {
 RankPlan rank_plan(int64_t M, int64_t Kd, int r_max, int G)
 {
     RankPlan pl;
-    pl.RP = r_max <= 32 ? 32 : 64;
+    pl.RP = rank_tc_pad(r_max);
     const int stage = RK_X_BYTES + G * pl.RP * 128;
     pl.S = (RK_SMEM_BUDGET - 2048) / stage;
     if (pl.S > RK_MAX_S) pl.S = RK_MAX_S;
@@ -485,7 +485,7 @@ struct RankEnv {
 bool rank_tc_applies(int64_t M, int64_t Kd, int r, const void *X, const void *W)
 {
     // Kd >= 64: the X box is never wider than the tensor
-    return M >= 1 && Kd >= RK_K && Kd % 8 == 0 && r >= 1 && r <= 64 && aligned16(X) && aligned16(W) &&
+    return M >= 1 && Kd >= RK_K && Kd % 8 == 0 && r >= 1 && r <= 128 && aligned16(X) && aligned16(W) &&
            (M + RK_M - 1) / RK_M * 64 <= 0x7FFFFFFF && Kd <= (int64_t(1) << 31);
 }
 
@@ -505,6 +505,7 @@ qerl_status rank_tc(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const RankOut
         if (!rank_tc_applies(M, Kd, outs[g].r, X, outs[g].W)) return QERL_ERR_SHAPE;
         r_max = outs[g].r > r_max ? outs[g].r : r_max;
     }
+    if (G * rank_tc_pad(r_max) > 256) return QERL_ERR_SHAPE;  // MMA N and TMEM columns
     const RankPlan pl = rank_plan(M, Kd, r_max, G);
     RankMaps maps;
     // X: [M, Kd] bf16, 128 tokens x 64 k per box; W_g: [r_g, Kd], RP rows x 64 k
@@ -531,7 +532,7 @@ qerl_status rank_tc(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const RankOut
     static const RankEnv env;
     p.timeout_ns = env.timeout_ns;
     const unsigned grid = (unsigned)((int64_t)pl.m_tiles * pl.splits);
-    auto kernel = pl.RP == 32 ? rank_tc_kernel<32> : rank_tc_kernel<64>;
+    auto kernel = pl.RP == 32 ? rank_tc_kernel<32> : pl.RP == 64 ? rank_tc_kernel<64> : rank_tc_kernel<128>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) != cudaSuccess)
         return QERL_ERR_CUDA;
     return launched(launch_k(kernel, dim3(grid), dim3(RK_THREADS), pl.smem, s, chain, maps, p));

@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("M,K,N,r", [(65, 256, 128, 1), (128, 512, 64, 5), (129, 256, 200, 31), (300, 1280, 136, 33),
-                                     (1000, 768, 128, 64), (65, 16384, 128, 32)])
+                                     (1000, 768, 128, 64), (65, 16384, 128, 32), (300, 512, 136, 128),
+                                     (130, 256, 64, 100), (200, 512, 72, 65)])
 def test_forward_t_many_tokens(M, K, N, r):
     c = LinearCase(M, K, N, r, config=9, idx=M + r).quantize_gpu()
     t = torch.empty(M, r, dtype=torch.float32, device="cuda")
@@ -72,8 +73,10 @@ def test_backward_rank_matches_cuda_cores():
         assert_rel_rms(f64(a), f64(b), 5e-5, name)
 
 
-@pytest.mark.parametrize("M,Ns,r", [(200, [128, 256, 64], 12), (130, [136, 72], 40), (1000, [256, 128, 128], 32)])
+@pytest.mark.parametrize("M,Ns,r", [(200, [128, 256, 64], 12), (130, [136, 72], 40), (1000, [256, 128, 128], 32),
+                                    (200, [128, 256, 64], 96)])
 def test_grouped_t_many_tokens(M, Ns, r):
+    """r = 96 pads to 128 ranks per group: two groups per pass over x, then one."""
     K = 512
     cases = [LinearCase(M, K, N, r, config=9, idx=40 + i).quantize_gpu() for i, N in enumerate(Ns)]
     x = cases[0].x
