@@ -34,8 +34,8 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes (read + write) per launch of the forward kernel, from one ncu capture
 # (profiles/tc_fwd_decode_qwen7b_m64.md) of csrc/linear_tc.cu with this sha256
 # prefix; reported as roofline.traffic only while the source still matches.
-NCU_KERNEL_SHA = "9e581bbf41b7808f"
-NCU_DRAM_BYTES = {"gate_proj": 39.93856e6, "up_proj": 39.938304e6, "down_proj": 42.155776e6}
+NCU_KERNEL_SHA = "883e2b82deff5143"
+NCU_DRAM_BYTES = {"gate_proj": 39.939072e6, "up_proj": 39.938304e6, "down_proj": 42.14656e6}
 
 
 def ncu_traffic(name):
