@@ -330,8 +330,9 @@ qerl_status simt_fwd(const FwdArgs &a, char *ws, cudaStream_t s)
 
 // ------------------------------------------------------------ thin products
 // The LoRA products of the backward have one side of width r <= 64 and a long
-// reduction; they are HBM-bound.  Two CUDA-core kernels, split over the
-// reduction (partials summed in split order by split_reduce):
+// reduction; they are HBM-bound.  The tensor-core kernels of rank_tc.cu run
+// them where their shape allows; these two CUDA-core kernels cover the rest,
+// split over the reduction (partials summed in split order by split_reduce):
 //   rows x rank:   P[z][m][j] = sum_{k in split z} X[m, k] * W(k, j)
 //                  X bf16 [M, Kd] row-major; W(k, j) = Wkj[k * r + j] or Wjk[j * Kd + k]
 //   wide x rank:   P[z][w][j] (or [j][w]) = sum_{m in split z} D[m, w] * T[m, j]
@@ -633,9 +634,9 @@ __global__ void __launch_bounds__(256) u_reduce_kernel(const UReduceGroups grp, 
 // out = alpha * P (+ out if accumulate), P[w][j] (wj) or P[j][w] = sum over m
 // of D[m, w] T[m, j]: the tensor-core wide product, then the split reduction.
 qerl_status wide_rows(const __nv_bfloat16 *D, int64_t M, int64_t Wd, const float *T, int r, bool wj, StoreF32 ep,
-                      __nv_bfloat16 *tb, float *part, cudaStream_t s)
+                      __nv_bfloat16 *tb, bool tb_ready, float *part, cudaStream_t s)
 {
-    QERL_TRY(wide_tc(D, M, Wd, T, r, wj, tb, part, g_chain.load() != 0, s));
+    QERL_TRY(wide_tc(D, M, Wd, T, r, wj, tb, tb_ready, part, g_chain.load() != 0, s));
     const int64_t P = wj ? Wd : r, Q = wj ? r : Wd;
     int64_t g = (P * Q + 255) / 256;
     if (g > 8 * num_sms()) g = 8 * num_sms();
@@ -652,18 +653,58 @@ __global__ void __launch_bounds__(256) transpose_rank_kernel(const __nv_bfloat16
         for (int j = 0; j < r; ++j) bt[(int64_t)j * N + n] = B[n * r + j];
 }
 
-// out = alpha * X W^T (+ out if accumulate) with W [r, Kd]: the tensor-core
-// rank product, then the split reduction.
-qerl_status rank_rows(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const __nv_bfloat16 *W, int r, StoreF32 ep,
-                      float *part, cudaStream_t s)
+// The sum T [M, r] of a rank product's split partials (split order) -> out, and
+// in the same pass what the next products read: the bf16 pair Tb [M][2 RP] of
+// the wide products (hi = bf16(T), lo = bf16(T - hi), zeros past r) when tb is
+// given, and the dx kernel's LoRA operand v' = bf16(s T / (s_t 2^c)) [M, vp_pad]
+// (zeros past r) when vp is given.
+__global__ void __launch_bounds__(256) rank_reduce_kernel(const float *__restrict__ part, int splits, int64_t M, int r,
+                                                          float *__restrict__ out, __nv_bfloat16 *__restrict__ tb,
+                                                          int RP, __nv_bfloat16 *__restrict__ vp, int vp_pad, float s,
+                                                          const float *__restrict__ tensor_scale)
 {
+    pdl_trigger();
+    pdl_wait();
+    const int jw = RP > vp_pad ? RP : vp_pad;  // columns per row (>= r)
+    float fac = 0.0f;
+    if (vp) {
+        const float st = *tensor_scale;
+        fac = s / (st * pow2f(tc_exponent_offset(st)));
+    }
+    const int64_t n = M * jw;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / jw;
+        const int j = (int)(i % jw);
+        float t = 0.0f;
+        if (j < r) {
+            t = sum_splits(part + m * r + j, M * r, splits);
+            out[m * r + j] = t;
+        }
+        if (tb && j < RP) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(t);
+            tb[m * 2 * RP + j] = hi;
+            tb[m * 2 * RP + RP + j] = __float2bfloat16_rn(t - __bfloat162float(hi));
+        }
+        if (vp && j < vp_pad) vp[m * vp_pad + j] = __float2bfloat16_rn(j < r ? t * fac : 0.0f);
+    }
+}
+
+// T = X W^T with W [r, Kd] on tensor cores, reduced by rank_reduce_kernel into
+// out [M, r] (and Tb, v' where given).
+qerl_status rank_rows_reduce(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const __nv_bfloat16 *W, int r,
+                             float *out, __nv_bfloat16 *tb, __nv_bfloat16 *vp, int vp_pad, float s,
+                             const float *tensor_scale, float *part, cudaStream_t st)
+{
+    const bool chain = g_chain.load() != 0;
     const RankOut o{W, r, part};
-    QERL_TRY(rank_tc(X, M, Kd, &o, 1, g_chain.load() != 0, s));
-    int64_t g = (M * r + 255) / 256;
+    QERL_TRY(rank_tc(X, M, Kd, &o, 1, chain, st));
+    const int RP = tb ? rank_tc_pad(r) : 0;
+    const int jw = std::max(std::max(RP, vp ? vp_pad : 0), r);
+    int64_t g = (M * jw + 255) / 256;
     if (g > 8 * num_sms()) g = 8 * num_sms();
-    split_reduce<<<(unsigned)g, 256, 0, s>>>(part, rank_tc_splits(M, Kd), M, r, ep.out, ep.ld, ep.alpha,
-                                             ep.accumulate);
-    return launched();
+    return launched(launch_k(rank_reduce_kernel, dim3((unsigned)g), dim3(256), 0, st, chain, (const float *)part,
+                             rank_tc_splits(M, Kd), M, r, out, tb, RP > 0 ? RP : r, vp, vp ? vp_pad : 0, s,
+                             tensor_scale));
 }
 
 // Scratch of the backward: v, t (when not saved), v' for the tensor-core dx,
@@ -696,9 +737,10 @@ BwdWs bwd_ws(int64_t M, int64_t N, int64_t K, int r)
     return w;
 }
 
-// v = dy B, dx (tensor cores where the shape allows, else CUDA cores), then
-// dA = s v^T x and dB = s dy^T t on CUDA cores (thin, HBM-bound products,
-// split over k when their outputs are too small to fill the GPU).
+// v = dy B, dx, then dA = s v^T x and dB = s dy^T t.  Each product runs on the
+// tensor cores where its shape allows (rank_tc.cu for the four rank-r products,
+// split over their long reduction and summed in split order; tc_dx for dx),
+// else on the CUDA-core kernels of this file.
 qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
 {
     const BwdWs w = bwd_ws(a.M, a.N, a.K, a.r);
@@ -718,20 +760,28 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     // the wide x rank products (dA, dB) on tensor cores
     const bool wide = thin && g_algo.load() != QERL_ALGO_SIMT && wide_tc_applies(a.M, a.K, a.r, a.x) &&
                       wide_tc_applies(a.M, a.N, a.r, a.dy);
+    const bool dx_tc = a.dx && g_algo.load() != QERL_ALGO_SIMT && tc_dx_applies(a.M, a.N, a.K, a.r);
+    bool vp_ready = false, tb_v = false;  // written by the reduction of v
     if (rank) {
         int64_t g = (a.N + 255) / 256;
         if (g > 4 * num_sms()) g = 4 * num_sms();
         transpose_rank_kernel<<<(unsigned)g, 256, 0, s>>>(a.B, a.N, a.r, bt);
         QERL_TRY(launched());
-        QERL_TRY(rank_rows(a.dy, a.M, a.N, bt, a.r, StoreF32{v, a.r, 1.0f, 0}, part, s));
+        // v, and in the same pass its bf16 pair (dA) and v' (dx)
+        __nv_bfloat16 *tbv = wide && a.dA ? tb : nullptr;
+        __nv_bfloat16 *vpv = dx_tc ? reinterpret_cast<__nv_bfloat16 *>(vp) : nullptr;
+        QERL_TRY(rank_rows_reduce(a.dy, a.M, a.N, bt, a.r, v, tbv, vpv, tc_dx_rpad(a.r), a.lora_scale,
+                                  a.tensor_scale, part, s));
+        vp_ready = vpv != nullptr;
+        tb_v = tbv != nullptr;
     } else if (thin)
         QERL_TRY(thin_rows(a.dy, a.M, a.N, a.B, false, a.r, StoreF32{v, a.r, 1.0f, 0}, part, s));
     else
         QERL_TRY(run_gemm_store(a.M, a.r, a.N, RowBF16{a.dy, a.N}, ColBF16{a.B, a.r}, StoreF32{v, a.r, 1.0f, 0},
                                 part, s));
     if (a.dx) {
-        if (g_algo.load() != QERL_ALGO_SIMT && tc_dx_applies(a.M, a.N, a.K, a.r))
-            QERL_TRY(tc_dx(a, v, vp, s));
+        if (dx_tc)
+            QERL_TRY(tc_dx(a, v, vp, vp_ready, s));
         else
             QERL_TRY(run_gemm(a.M, a.K, a.N, RowBF16{a.dy, a.N}, WCol{a.codes, a.scales, a.K, a.packed},
                               DxEpi{a.dx, a.K, a.tensor_scale, v, a.A, a.r, a.lora_scale}, s));
@@ -739,7 +789,7 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     if (a.dA) {
         const StoreF32 ep{a.dA, a.K, a.lora_scale, a.accumulate};
         if (wide)
-            QERL_TRY(wide_rows(a.x, a.M, a.K, v, a.r, false, ep, tb, part, s));
+            QERL_TRY(wide_rows(a.x, a.M, a.K, v, a.r, false, ep, tb, tb_v, part, s));
         else if (thin)
             QERL_TRY(thin_wide(a.x, a.M, a.K, v, a.r, false, ep, part, s));
         else
@@ -747,10 +797,14 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
     }
     if (a.dB) {
         const float *uu = a.t_saved;
+        bool tb_t = false;  // written by the reduction of t
         if (!uu) {
-            if (rank)
-                QERL_TRY(rank_rows(a.x, a.M, a.K, a.A, a.r, StoreF32{u, a.r, 1.0f, 0}, part, s));
-            else if (thin)
+            if (rank) {  // t, and in the same pass its bf16 pair (dB)
+                __nv_bfloat16 *tbt = wide ? tb : nullptr;
+                QERL_TRY(rank_rows_reduce(a.x, a.M, a.K, a.A, a.r, u, tbt, nullptr, 0, 0.0f, a.tensor_scale, part,
+                                          s));
+                tb_t = tbt != nullptr;
+            } else if (thin)
                 QERL_TRY(thin_rows(a.x, a.M, a.K, a.A, true, a.r, StoreF32{u, a.r, 1.0f, 0}, part, s));
             else
                 QERL_TRY(run_gemm_store(a.M, a.r, a.K, RowBF16{a.x, a.K}, RowBF16{a.A, a.K},
@@ -759,7 +813,7 @@ qerl_status run_bwd(const BwdArgs &a, char *ws, cudaStream_t s)
         }
         const StoreF32 ep{a.dB, a.r, a.lora_scale, a.accumulate};
         if (wide)
-            QERL_TRY(wide_rows(a.dy, a.M, a.N, uu, a.r, true, ep, tb, part, s));
+            QERL_TRY(wide_rows(a.dy, a.M, a.N, uu, a.r, true, ep, tb, tb_t, part, s));
         else if (thin)
             QERL_TRY(thin_wide(a.dy, a.M, a.N, uu, a.r, true, ep, part, s));
         else

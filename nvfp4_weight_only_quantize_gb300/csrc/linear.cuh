@@ -76,15 +76,17 @@ qerl_status rank_tc(const __nv_bfloat16 *X, int64_t M, int64_t Kd, const RankOut
 // Wide x rank products on tensor cores (rank_tc.cu), split over the tokens:
 //   part[z][w][j] (wj) or part[z][j][w] = sum over m in split z of D[m, w] * T[m, j],
 // D bf16 [M, Wd] row-major, 16-byte aligned, Wd % 8 == 0, Wd >= 64; T FP32
-// [M, r], r <= 64.  tb holds wide_tc_tb_bytes(M, r) bytes of scratch (T as a
-// bf16 hi/lo pair), part wide_tc_part_bytes(M, Wd, r); the wide_tc_splits(M, Wd)
-// partials are summed in split order by the caller.
+// [M, r], r <= 64.  tb holds wide_tc_tb_bytes(M, r) bytes of scratch: T as the
+// bf16 pair [M][2 RP] (hi = bf16(T), lo = bf16(T - hi), zeros past r; RP =
+// rank_tc_pad(r)), written here unless tb_ready.  part holds
+// wide_tc_part_bytes(M, Wd, r) bytes; the wide_tc_splits(M, Wd) partials are
+// summed in split order by the caller.
 bool wide_tc_applies(int64_t M, int64_t Wd, int r, const void *D);
 int wide_tc_splits(int64_t M, int64_t Wd);
 size_t wide_tc_part_bytes(int64_t M, int64_t Wd, int r);
 size_t wide_tc_tb_bytes(int64_t M, int r);
 qerl_status wide_tc(const __nv_bfloat16 *D, int64_t M, int64_t Wd, const float *T, int r, bool wj,
-                    __nv_bfloat16 *tb, float *part, bool chain, cudaStream_t s);
+                    __nv_bfloat16 *tb, bool tb_ready, float *part, bool chain, cudaStream_t s);
 
 // LoRA down-projection for many tokens, for G (<= 3) linears sharing x (one
 // pass over x on tensor cores where rank_tc applies, else CUDA cores group by
@@ -104,10 +106,13 @@ qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const D
 
 // Tensor-core input gradient dx = dy w_hat + s v A for the shapes it covers
 // (K % 256 == 0, N % 64 == 0, r <= 256); v = dy B in FP32 [M, r] is given, and
-// vp_ws holds tc_dx_ws_bytes(M, r) bytes of scratch.
+// vp_ws holds tc_dx_ws_bytes(M, r) bytes of scratch: the LoRA operand
+// v' = bf16(s v / (s_t 2^c)) as [M, tc_dx_rpad(r)] (zeros past r), written here
+// unless vp_ready.
 bool tc_dx_applies(int64_t M, int64_t N, int64_t K, int r);
+int tc_dx_rpad(int r);
 size_t tc_dx_ws_bytes(int64_t M, int r);
-qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, cudaStream_t s);
+qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, bool vp_ready, cudaStream_t s);
 
 // Forward with a fixed scratch buffer: validates the arguments like the
 // workspace entry point, returns QERL_ERR_TOO_LARGE when the call needs more

@@ -369,17 +369,15 @@ bool tc_dx_applies(int64_t M, int64_t N, int64_t K, int r)
            M <= (1 << 30) && N <= (1 << 30) && K <= (1 << 30);
 }
 
-size_t tc_dx_ws_bytes(int64_t M, int r)
-{
-    const int r_pad = (r + BX_N - 1) / BX_N * BX_N;
-    return round256(size_t(M) * r_pad * 2);
-}
+int tc_dx_rpad(int r) { return (r + BX_N - 1) / BX_N * BX_N; }
 
-qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, cudaStream_t s)
+size_t tc_dx_ws_bytes(int64_t M, int r) { return round256(size_t(M) * tc_dx_rpad(r) * 2); }
+
+qerl_status tc_dx(const BwdArgs &a, const float *v, char *vp_ws, bool vp_ready, cudaStream_t s)
 {
-    const int r_pad = (a.r + BX_N - 1) / BX_N * BX_N;
+    const int r_pad = tc_dx_rpad(a.r);
     __nv_bfloat16 *vp = reinterpret_cast<__nv_bfloat16 *>(vp_ws);
-    {
+    if (!vp_ready) {
         int64_t g = (a.M * r_pad + 255) / 256;
         if (g > 4 * num_sms()) g = 4 * num_sms();
         vprime_kernel<<<(unsigned)g, 256, 0, s>>>(v, (int)a.M, a.r, r_pad, a.lora_scale, a.tensor_scale, vp);

@@ -555,11 +555,11 @@ size_t wide_tc_part_bytes(int64_t M, int64_t Wd, int r)
 size_t wide_tc_tb_bytes(int64_t M, int r) { return round256(size_t(M) * 2 * (r <= 32 ? 32 : 64) * 2); }
 
 qerl_status wide_tc(const __nv_bfloat16 *D, int64_t M, int64_t Wd, const float *T, int r, bool wj,
-                    __nv_bfloat16 *tb, float *part, bool chain, cudaStream_t s)
+                    __nv_bfloat16 *tb, bool tb_ready, float *part, bool chain, cudaStream_t s)
 {
     if (!wide_tc_applies(M, Wd, r, D)) return QERL_ERR_SHAPE;
     const WidePlan pl = wide_plan(M, Wd, r);
-    {
+    if (!tb_ready) {
         int64_t g = (M * pl.RP + 255) / 256;
         if (g > 4 * num_sms()) g = 4 * num_sms();
         QERL_TRY(launched(launch_k(hilo_kernel, dim3((unsigned)g), dim3(256), 0, s, chain, T, M, r, pl.RP, tb)));
