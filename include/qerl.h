@@ -227,12 +227,16 @@ qerl_status qerl_nvfp4_unpack_codes(const uint8_t *packed, int64_t N, int64_t K,
  * q|k|v and gate|up read one normalised input) in one call; the same result as
  * qerl_nvfp4_lora_linear_fwd (or _packed) on each group.  The pages have no
  * such call: it is an interface of this library that saves launches.  The
- * tensor-core path serves up to 3 groups in one launch; more groups, or shapes
- * it does not cover, run the groups one after the other.
+ * tensor-core path serves up to 3 groups in one launch (above 64 tokens, one
+ * pass over x also computes every group's LoRA down-projection); more groups,
+ * or shapes it does not cover, run the groups one after the other.
  *   groups (host) [n_groups], 1 <= n_groups <= 8: per group N, codes, scales,
  *   tensor_scale, A [r, K], B [N, r], y [M, N] out, t_out optional [M, r].
  *   x (device) bf16 [M, K]; r, lora_scale and packed (0: standard codes,
  *   1: packed layout) shared.  ws (device) >= qerl_lora_linear_fwd_grouped_ws_bytes.
+ * Errors: QERL_ERR_INVALID_ARG for n_groups outside 1..8 or packed not 0/1;
+ * each group is checked as in qerl_nvfp4_lora_linear_fwd (the same statuses,
+ * nothing launched); QERL_ERR_WORKSPACE for a short ws.
  */
 typedef struct qerl_lora_linear_group {
     int64_t N;
