@@ -65,6 +65,38 @@ def test_argument_errors_return_before_any_launch(L):
     assert L.qerl_set_linear_algo(9) == 1
 
 
+def test_grouped_argument_errors_return_before_any_launch(L):
+    fake = 1 << 20  # never dereferenced
+    g = q._Group(16, fake, fake, fake, fake, fake, fake, None)
+    arr = (q._Group * 2)(g, g)
+    ptr = C.cast(arr, C.c_void_p)
+
+    def call(x, K, r, groups, n, packed, wsb):
+        return L.qerl_nvfp4_lora_linear_fwd_grouped(x, 8, K, r, 2.0, groups, n, packed, fake, wsb, None)
+    assert call(fake, 32, 4, None, 2, 0, 1 << 30) == 1      # no group array
+    assert call(fake, 32, 4, ptr, 0, 0, 1 << 30) == 1       # n_groups outside 1..8
+    assert call(fake, 32, 4, ptr, 9, 0, 1 << 30) == 1
+    assert call(fake, 32, 4, ptr, 2, 2, 1 << 30) == 1       # packed flag
+    assert call(fake, 32, 0, ptr, 2, 0, 1 << 30) == 2       # r outside 1..256
+    assert call(fake, 40, 4, ptr, 2, 0, 1 << 30) == 2       # K % 16
+    assert call(fake + 8, 32, 4, ptr, 2, 0, 1 << 30) == 3   # misaligned x
+    assert call(fake, 32, 4, ptr, 2, 0, 0) == 8             # short workspace
+    bad = (q._Group * 2)(g, q._Group(16, fake + 4, fake, fake, fake, fake, fake, None))
+    assert call(fake, 32, 4, C.cast(bad, C.c_void_p), 2, 0, 1 << 30) == 3  # misaligned codes of group 1
+
+
+def test_workspace_covers_every_region(L):
+    """Lower bounds from the regions each call keeps in its workspace."""
+    M, K, r = 4096, 5120, 32
+    Ns = [5120, 1024, 1024]
+    # grouped forward above 64 tokens: u per group (bf16 [M, 64]) + one partial slice per group
+    assert q.grouped_ws_bytes(M, K, r, Ns) >= 3 * M * 64 * 2 + 3 * M * r * 4
+    assert q.grouped_ws_bytes(M, K, 128, Ns) >= 3 * M * 128 * 2 + 3 * M * 128 * 4
+    # backward: v and t (FP32), v' (bf16 [M, 64]), B^T (bf16 [r, N]), hi/lo pair (bf16 [M, 64]), partials
+    M, N, K = 8192, 3584, 3584
+    assert q.workspace_bytes(q.OP_LINEAR_BWD, M, N, K, r) >= 2 * M * r * 4 + M * 64 * 2 + r * N * 2 + M * 64 * 2
+
+
 def test_sigma_schedule_matches_oracle(L):
     for S in (1, 2, 5, 10):
         for T in (1, 7, 1000):
