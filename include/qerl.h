@@ -153,7 +153,9 @@ qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int6
  *     nothing launched.
  *   - Every call on a device shares the one buffer: calls whose kernels overlap
  *     on the GPU (other streams, other host threads) race and corrupt each
- *     other; serialize them.  The kernels clear what must start at zero.
+ *     other; serialize them.  The buffer holds the LoRA down-projection u and
+ *     the split-K partial tiles; each call writes every part of it that it
+ *     reads, so no part has to start at zero.
  */
 qerl_status qerl_nvfp4_lora_linear_fwd_noalloc(const void *x, int64_t M, int64_t K, int64_t N,
                                                const uint8_t *codes, const uint8_t *scales,

@@ -10,11 +10,13 @@
 namespace qerl {
 namespace {
 
-// The scratch of the no-allocation forward (split-K partials, tile counters,
-// the LoRA down-projection).  Every GPU that loads the library holds these
+// The scratch of the no-allocation forward: the LoRA down-projection u (and
+// its split partials for many tokens) and the split-K partial tiles.  Each
+// launch writes every scratch element it later reads, so nothing has to start
+// at zero.  Every GPU that loads the library holds these
 // QERL_NOALLOC_SCRATCH_BYTES until the process exits.  All calls on a device
-// share it and keep the previous call's contents; the kernels clear the tile
-// counters that must start at zero, and calls that overlap on the GPU race.
+// share it and keep the previous call's contents; calls that overlap on the
+// GPU race.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[QERL_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;

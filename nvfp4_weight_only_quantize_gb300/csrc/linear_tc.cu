@@ -30,9 +30,7 @@
 
 #include <atomic>
 #include <cstdlib>
-#include <map>
 #include <mutex>
-#include <numeric>
 #include <utility>
 
 #include "linear.cuh"
@@ -46,12 +44,7 @@ using namespace ptx;
 constexpr int BK = 64;          // k per MMA step: one 128-byte swizzle row of bf16
 constexpr int GK = 4;           // k-steps per raw stage (256 k)
 constexpr int TILE_N = 128;     // weight rows per CTA (MMA M)
-constexpr int DQ_GROUPS = 2;      // dequant groups; group g takes the stages j = g (mod DQ_GROUPS)
 constexpr int DQ_GROUP_WARPS = 4; // one warp per 32 weight rows of the tile
-constexpr int NUM_DQ_WARPS = DQ_GROUPS * DQ_GROUP_WARPS;
-static_assert(DQ_GROUPS == 2, "the epilogue and TMEM budget assume two dequant groups");
-constexpr int WARP_RAW = NUM_DQ_WARPS, WARP_X = NUM_DQ_WARPS + 1, WARP_MMA = NUM_DQ_WARPS + 2;
-constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
 constexpr int RAW_CODES = TILE_N * GK * BK / 2;    // 16 KB: 128 rows x 128 code bytes (SW128)
 constexpr int RAW_SCALES = TILE_N * GK * BK / 16;  // 2 KB: 128 rows x 16 scale bytes
 constexpr int RAW_STAGE = RAW_CODES + RAW_SCALES;  // 18 KB, a multiple of 1024
@@ -65,21 +58,28 @@ constexpr int MAX_SPLITS = 8;  // split-K factor cap: bounds the partial traffic
 constexpr int FUSED_R = 32;  // LoRA rows loaded per k-step in fused mode
 template <int BN, bool FUSED = false>
 struct Cfg {
-    // k-steps per pipeline stage: every stage costs the MMA issuer one barrier
-    // round trip and one commit, so small token tiles (short MMAs) take two.
-    static constexpr int SPS = BN >= 256 ? 2 : 4;
+    // Dequant groups of four warps; group g takes the stages j = g (mod DQG).
+    // Decode tiles (short MMAs, HBM-bound) run three groups on half-size
+    // stages, so that more stages are being dequantized at once and each group
+    // finds a free stage; wide tiles keep two.
+    static constexpr int DQG = BN <= 64 ? 3 : 2;
+    static constexpr int NUM_DQ_WARPS = DQG * DQ_GROUP_WARPS;
+    static constexpr int WARP_RAW = NUM_DQ_WARPS, WARP_X = NUM_DQ_WARPS + 1, WARP_MMA = NUM_DQ_WARPS + 2;
+    static constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
+    // k-steps per pipeline stage (2 = 128 k, 4 = 256 k).
+    static constexpr int SPS = (BN >= 256 || BN <= 64) ? 2 : 4;
     // A stage holds SPS k-steps of the dequantized weight tile (TMEM); at least
-    // DQ_GROUPS of them, so a group never waits on a stage two mbarrier phases
-    // ahead of the MMA (parity aliasing).
-    // One more stage than dequant groups (where TMEM allows): a group can fill a
-    // free stage while the MMA still reads the one it filled before.
-    static constexpr int S = SPS == 4 ? 3 : 4;
-    static_assert(S >= DQ_GROUPS, "parity waits need at least one stage per dequant group");
+    // DQG of them, so a group never waits on a stage two mbarrier phases ahead
+    // of the MMA (parity aliasing).  More stages than groups (where TMEM
+    // allows): a group can fill a free stage while the MMA still reads the ones
+    // filled before.
+    static constexpr int S = BN <= 64 ? 6 : (SPS == 4 ? 3 : 4);
+    static_assert(S >= DQG, "parity waits need at least one stage per dequant group");
     // Token-tile stages (smem), deeper than the A ring: a token slot is reloaded
     // only after the MMA that read it completed, a ~2 us round trip.
-    static constexpr int XS = FUSED ? 3 : (BN >= 128 ? 2 : 4);
+    static constexpr int XS = BN <= 64 ? (FUSED ? 6 : 8) : (BN >= 128 ? 2 : 4);
     static constexpr int R = 4;  // raw (code+scale) stages
-    static_assert(GK % SPS == 0 && GK / SPS <= DQ_GROUPS, "each group has at most one stage per raw stage");
+    static_assert(GK % SPS == 0 && GK / SPS <= DQG, "each group has at most one stage per raw stage");
     static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
     static_assert(R * GK >= S * SPS, "raw ring deep enough for parity-safe waits");
     static constexpr int X_STEP = BN * BK * 2;
@@ -133,8 +133,6 @@ struct TcFwdParams {
     int fault;           // test hook: CTA 0 withholds one arrival so its waits time out
     int chain;           // launched chained: token tiles and B wait for the preceding grid
     float lora_scale;    // fused: s
-    int cs;              // CTAs per cluster (1, 2 or 4): consecutive weight tiles sharing one
-                         // token tile per stage, each CTA loading 1/cs of it for all (multicast)
 };
 
 
@@ -189,11 +187,13 @@ __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
 }
 
 template <int BN, bool PACKED, bool FUSED>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
     tc_fwd_kernel(const __grid_constant__ TcMaps maps, const TcFwdParams p)
 {
     using C = Cfg<BN, FUSED>;
     constexpr int SPS = C::SPS;
+    constexpr int DQG = C::DQG, NUM_DQ_WARPS = C::NUM_DQ_WARPS;
+    constexpr int WARP_RAW = C::WARP_RAW, WARP_X = C::WARP_X, WARP_MMA = C::WARP_MMA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *X_ring = smem;
@@ -213,12 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int *ep_ok = abort_flag + 1;  // [4]: epilogue warps' view of acc_full
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // blockIdx.x = (split * m_tiles + m_tile) * n_tiles + n_tile; n_tiles % cs == 0, so
-    // the CTAs of a cluster share split and m_tile (the same token tiles) and the
-    // cluster rank is n_tile % cs.
-    const int cs = p.cs;
-    const uint32_t crank = cs > 1 ? cluster_ctarank() : 0u;
-    const uint16_t cmask = (uint16_t)((1u << cs) - 1u);
+    // blockIdx.x = (split * m_tiles + m_tile) * n_tiles + n_tile
     const int n_tile = blockIdx.x % p.n_tiles;
     const int m_tile = (blockIdx.x / p.n_tiles) % p.m_tiles;
     const int split = blockIdx.x / (p.n_tiles * p.m_tiles);
@@ -244,10 +239,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int n_stages = (n_steps + SPS - 1) / SPS;  // the last (LoRA) stage may be partial
     const int main_stages = n_main / SPS;
     // Every CTA walks its k-range from a different raw group, so that the CTAs
-    // do not all read the same token tile from L2 at the same time.
-    // The rotation is shared by each aligned group of four weight tiles (so by
-    // every cluster) and does not depend on the cluster size: the summation
-    // order, hence the result, is the same for every cluster size.
+    // do not all read the same token tile from L2 at the same time.  The
+    // rotation fixes the summation order, hence the result, per weight tile.
     const int grot = n_groups > 0 ? ((n_tile >> 2) * 5 + m_tile * 3) % n_groups : 0;
     // k-step of the CTA's i-th main step.  No division: the producers run on one
     // lane that shares its SM sub-partition with issue-bound dequantizing warps,
@@ -265,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < C::XS; ++i) {
             mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], (uint32_t)cs);  // every CTA of the cluster frees the slot
+            mbar_init(&x_empty[i], 1);
         }
         for (int i = 0; i < C::S; ++i) {
             mbar_init(&a_full[i], DQ_GROUP_WARPS);
@@ -292,25 +285,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    if (cs > 1)
-        cluster_sync();  // every CTA's barriers are initialised before any multicast reaches them
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_trigger();  // a chained successor may be scheduled (it waits for this grid before touching memory)
     const unsigned long long deadline = globaltimer_ns() + p.timeout_ns;
 
     // Bounded wait for the phase with this parity; false once the CTA aborts.
-    // Waiting threads poll with a short sleep between tries rather than
-    // spinning: a spinning waiter takes the dequantizing warps' issue slots.
-    const unsigned sleep_ns = warp >= NUM_DQ_WARPS ? 64u : 32u;
+    // A waiting thread is suspended in hardware until the phase completes (or
+    // the hint runs out): it takes no issue slots from the dequantizing warps
+    // and resumes as soon as the phase completes.
     auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         if (mbar_try_wait(bar, parity)) return true;
         for (;;) {
             if (*abort_flag) return false;
-            __nanosleep(sleep_ns);
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
             if (globaltimer_ns() > deadline) {
                 *abort_flag = 1;
                 latch_error(p.err, QERL_ERR_TIMEOUT);
@@ -417,10 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int i = j * SPS + sub;
                     const CUtensorMap *map = i < n_main ? x_map : u_map;
                     const int kx = i < n_main ? kstep(i) * BK : (i - n_main) * BK;
-                    if (cs == 1)
-                        tma_load_2d_hint(dst + sub * C::X_STEP, map, &x_full[slot], kx, m0, pol);
-                    else if ((sub & (cs - 1)) == (int)crank)  // this CTA's share, to every CTA of the cluster
-                        tma_load_2d_multicast(dst + sub * C::X_STEP, map, &x_full[slot], kx, m0, cmask, pol);
+                    tma_load_2d_hint(dst + sub * C::X_STEP, map, &x_full[slot], kx, m0, pol);
                 }
                 issued = j + 1;
             }
@@ -465,10 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (FUSED && j == main_stages - 1) umma_commit(t_full);
                 umma_commit(&stage_empty[s]);
-                if (cs == 1)
-                    umma_commit(&x_empty[xs]);
-                else
-                    umma_commit_multicast(&x_empty[xs], cmask);  // the slot is free in this CTA
+                umma_commit(&x_empty[xs]);
             }
             __syncwarp();
             if (j + 1 < n_stages) {
@@ -482,7 +465,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------- dequantize
-        // Group g = warp / 4 takes the stages j = g, g + DQ_GROUPS, ...; thread =
+        // Group g = warp / 4 takes the stages j = g, g + DQG, ...; thread =
         // one weight row of the tile, all 64 k of each of the stage's SPS steps.
         const int row = (warp & 3) * 32 + lane;
         const int group = warp >> 2;
@@ -490,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool row_ok = n < Ng;
         const float pow2 = pow2f(126 - tc_exponent_offset(*tsg));
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        for (int j = group; j < n_stages; j += DQ_GROUPS) {
+        for (int j = group; j < n_stages; j += DQG) {
             const int s = j % C::S;
             const uint32_t sround = (uint32_t)(j / C::S);
             const bool main_stage = j < main_stages;
@@ -500,19 +483,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&stage_empty[s], (sround - 1) & 1u))) break;
             if (main_stage && !__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(g / C::R) & 1u))) break;
             const int nsub = min(SPS, n_steps - j * SPS);
+            // A main stage reads all of its codes and scales first (every load in
+            // flight at once), then hands the raw slot back to the producer
+            // before dequantizing from registers.
+            uint4 cw[2 * SPS];
+            uint32_t scw[SPS];
+            if (main_stage) {
+                const uint8_t *rb = R_ring + rs * RAW_STAGE;
+                const int q0 = (j * SPS) % GK;
+#pragma unroll
+                for (int sub = 0; sub < SPS; ++sub) {
+                    // codes: row `row`, logical 16-byte chunks 2q and 2q+1 of the
+                    // 128-byte row, stored by TMA at chunk ^ (row % 8)
+                    const int q = q0 + sub;
+                    cw[2 * sub] = *reinterpret_cast<const uint4 *>(rb + row * 128 + (((2 * q) ^ (row & 7)) * 16));
+                    cw[2 * sub + 1] =
+                        *reinterpret_cast<const uint4 *>(rb + row * 128 + (((2 * q + 1) ^ (row & 7)) * 16));
+                    scw[sub] = *reinterpret_cast<const uint32_t *>(rb + RAW_CODES + row * 16 + q * 4);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);
+            }
 #pragma unroll
             for (int sub = 0; sub < SPS; ++sub) {
                 if (sub >= nsub) break;
                 const int i = j * SPS + sub;
                 uint32_t out[32];
                 if (main_stage) {
-                    const int q = i % GK;
-                    // codes: row `row`, logical 16-byte chunks 2q and 2q+1 of the 128-byte
-                    // row, stored by TMA at chunk ^ (row % 8)
-                    const uint32_t rb = smem_u32(R_ring + rs * RAW_STAGE) + row * 128;
-                    const uint4 c0 = ld_shared_v4(rb + (uint32_t)(((2 * q) ^ (row & 7)) * 16));
-                    const uint4 c1 = ld_shared_v4(rb + (uint32_t)(((2 * q + 1) ^ (row & 7)) * 16));
-                    const uint32_t sc = ld_shared_u32(smem_u32(R_ring + rs * RAW_STAGE + RAW_CODES) + row * 16 + q * 4);
+                    const uint4 c0 = cw[2 * sub], c1 = cw[2 * sub + 1];
+                    const uint32_t sc = scw[sub];
                     const uint32_t f0 = scale_factor_bf16x2(sc << 20, pow2);
                     const uint32_t f1 = scale_factor_bf16x2(sc << 12, pow2);
                     const uint32_t f2 = scale_factor_bf16x2(sc << 4, pow2);
@@ -552,10 +551,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 // row `row` of the step's A tile: TMEM lane `row`, 32 columns of bf16 pairs
                 tmem_st32(trow + (uint32_t)(C::A_COL0 + s * 32 * SPS + sub * 32), out);
-            }
-            if (main_stage) {  // every group's stage is its only one in the raw stage
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[rs]);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -624,8 +619,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    // No CTA leaves while a peer may still multicast into it or arrive on its barriers.
-    if (cs > 1) cluster_sync();
 }
 
 // LoRA down-projection for the tensor-core path: t = x A^T (FP32), written as
@@ -818,14 +811,11 @@ bool tc_fwd_applies(int64_t M, int64_t N, int64_t K, int r)
 struct Env {
     unsigned long long timeout_ns = 2000000000ull;  // 2 s
     int fault = 0;
-    int cluster = 0;  // QERL_TC_CLUSTER = 1, 2 or 4 forces that cluster size (tests)
     int no_fuse = 0;  // QERL_TC_NO_FUSE = 1: separate down-projection grid always (tests)
     Env()
     {
         const char *nf = std::getenv("QERL_TC_NO_FUSE");
         if (nf && nf[0] == '1') no_fuse = 1;
-        const char *c = std::getenv("QERL_TC_CLUSTER");
-        if (c && (c[0] == '1' || c[0] == '2' || c[0] == '4') && c[1] == 0) cluster = c[0] - '0';
         const char *f = std::getenv("QERL_TEST_WITHHOLD_ARRIVAL");
         if (f && f[0] == '1') {
             fault = 1;
@@ -839,51 +829,6 @@ const Env &env()
     return e;
 }
 
-// Largest cluster size in {4, 2, 1} that divides every group's weight tiles
-// (`tile_unit` = the gcd of the groups' tile counts: the CTAs of a cluster share
-// one multicast of the token tiles, u included, so they must belong to one
-// linear) and still lets the whole grid be resident at once (clusters are
-// placed within one GPC).
-template <bool MULTICAST, typename Kernel>
-int pick_cluster(Kernel kernel, cudaLaunchConfig_t cfg, int tile_unit, unsigned grid)
-{
-    static std::mutex mu;
-    static std::map<std::pair<const void *, int>, int> max_clusters;  // (kernel, cs) -> resident clusters
-    int forced = env().cluster;
-    if (!forced && !MULTICAST) return 1;
-    for (int cs = 4; cs >= 2; cs /= 2) {
-        if (forced && cs != forced) continue;
-        if (tile_unit % cs != 0) continue;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), cs * 64 + dev);
-        int nc = 0;
-        {
-            std::lock_guard<std::mutex> lk(mu);
-            auto it = max_clusters.find(key);
-            if (it != max_clusters.end()) {
-                nc = it->second;
-            } else {
-                cudaLaunchAttribute at[1];
-                at[0].id = cudaLaunchAttributeClusterDimension;
-                at[0].val.clusterDim.x = (unsigned)cs;
-                at[0].val.clusterDim.y = 1;
-                at[0].val.clusterDim.z = 1;
-                cfg.attrs = at;
-                cfg.numAttrs = 1;
-                cfg.gridDim = dim3((unsigned)cs);
-                if (cudaOccupancyMaxActiveClusters(&nc, kernel, &cfg) != cudaSuccess) {
-                    cudaGetLastError();
-                    nc = 0;
-                }
-                max_clusters[key] = nc;
-            }
-        }
-        if (forced || (unsigned)(nc * cs) >= grid) return cs;
-    }
-    return 1;
-}
-
 template <int BN, bool FUSED>
 qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid, bool packed, bool pdl, cudaStream_t s)
 {
@@ -893,28 +838,19 @@ qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid,
         return QERL_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(C::NUM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
-    TcFwdParams p = p0;
-    // Decode-sized token tiles are cheap to load per CTA, and clusters would tie
-    // the CTAs' pipelines together; wide (prefill) tiles share them.
-    int unit = 0;
-    for (int g = 0; g < p.grp.G; ++g) unit = std::gcd(unit, p.grp.tile_start[g + 1] - p.grp.tile_start[g]);
-    p.cs = pick_cluster<(BN >= 256)>(kernel, cfg, unit, grid);
+    const TcFwdParams p = p0;
     // Programmatic dependent launch: the CTAs may start while the preceding
     // grid still runs and stream their (frozen) weights; the token producer and
-    // the epilogue wait for that grid with griddepcontrol.wait.  Clusters of
-    // p.cs CTAs share the token tiles (multicast).
-    cudaLaunchAttribute attr[2];
+    // the epilogue wait for that grid with griddepcontrol.wait.  Every CTA
+    // loads its own token tiles.
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)p.cs;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess) return QERL_ERR_CUDA;
     return launched();
 }

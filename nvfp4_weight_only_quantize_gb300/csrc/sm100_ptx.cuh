@@ -81,17 +81,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
         "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
         : "memory");
 }
-// As tma_load_2d_hint, delivered to the same shared-memory offset (and mbarrier
-// offset) of every CTA of the cluster whose bit is set in cta_mask.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
-                                                      uint16_t cta_mask, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-        : "memory");
-}
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
@@ -163,31 +152,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
-}
-
-// As umma_commit, arriving on the mbarrier at the same offset in every CTA of
-// the cluster whose bit is set in cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// ------------------------------------------------------------------ cluster
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Every thread of every CTA of the cluster: release this CTA's prior writes
-// (and mbarrier inits) to the cluster, then wait for all CTAs.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 32 lanes x 32 bit, 16 consecutive columns: thread i gets lane (base + i).

@@ -67,10 +67,8 @@ def test_grouped_with_t_outputs():
                                   (512, [512, 128, 128])])
 def test_grouped_many_tokens_and_many_groups(M, Ns):
     """More than 64 tokens: one launch, one down-projection pass for all groups;
-    more than three groups: the groups run one after the other.  With 256-token
-    tiles the CTAs may form clusters that share the token tiles: a cluster never
-    spans two groups (4 weight tiles in all, split 1 + 2 + 1, must not cluster),
-    and groups whose tile counts allow it still cluster inside each group."""
+    more than three groups: the groups run one after the other.  Group tile
+    counts of 1 + 2 + 1 check that every CTA picks its own group's maps."""
     K, r = 512, 8
     cases, x, gs = _groups(M, K, Ns, r, False, seed=5)
     for c in cases:
