@@ -306,6 +306,80 @@ qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, uint32_t lay
 float qerl_aqn_sigma(int64_t step, int64_t total_steps, float sigma_start, float sigma_end,
                      int num_stages);
 
+/*
+ * Decoder-layer chain at decode batch sizes: every NVFP4 + LoRA linear of n
+ * Qwen2.5-style decoder layers, with the AQN-RMSNorms, the residual adds and
+ * SwiGLU between them, in one persistent launch (one CTA per SM).  The chain
+ * is the rollout forward the pages put the NVFP4 speed-up in ("QeRL" README
+ * "Highlights": rollout phase; 1kpapers abstract: 32B RL on one GPU); the
+ * norm is AQN-RMSNorm (1kpapers abstract; dataforcee "QERL: NVFP4-intensive
+ * learning", AQN paragraph: the noise lives in the norm's scale).  Per layer:
+ *     h1 = h0 + attn W_o^T (+ LoRA),   q,k,v = N1(h0) W_{q,k,v}^T (+ LoRA),
+ *     h2 = h1 + (silu(N2(h1) W_gate^T) * N2(h1) W_up^T) W_down^T (+ LoRA each),
+ * N_i(h) = h * rsqrt(mean(h^2) + eps) * (gamma_i + sigma z_i), z ~ N(0,1) per
+ * channel from Philox4x64-10 (key (seed, 2*layer + i - 1), counter
+ * (channel / 4, step, 0, 0)), as qerl_aqn_rmsnorm (Box-Muller in FP32 here).
+ * Attention itself is outside the path: `attn` is its output, given.  Each
+ * linear's output is rounded to bf16, residual sums are rounded to bf16.
+ * The norm is fused: its producer writes bf16(h * (gamma + sigma z)) and the
+ * consumer scales its output rows by rsqrt(mean(h^2) + eps).
+ */
+typedef struct {
+    const uint8_t *codes;       /* [N, K/2] E2M1 codes, packed layout (qerl_nvfp4_pack_codes) */
+    const uint8_t *scales;      /* [N, K/16] E4M3 block scales */
+    const float *tensor_scale;  /* device, 1 */
+    const void *A;              /* bf16 [r, K] LoRA down */
+    const void *B;              /* bf16 [N, r] LoRA up */
+} qerl_linear_weights;
+
+typedef struct {
+    qerl_linear_weights q, k, v, o, gate, up, down;
+    const void *gamma_attn;     /* bf16 [hidden]: scale of the norm before q, k, v */
+    const void *gamma_mlp;      /* bf16 [hidden]: scale of the norm before gate, up */
+    const void *attn;           /* bf16 [M, hidden]: attention output, the o input */
+    void *q_out, *k_out, *v_out;  /* bf16 [M, q_dim], [M, kv_dim] x 2, or NULL (scratch) */
+} qerl_decoder_layer;
+
+typedef struct {
+    int64_t M;                  /* tokens, 1..64 */
+    int64_t hidden;             /* multiple of 256; q_dim == hidden */
+    int64_t q_dim, kv_dim;      /* multiples of 128 */
+    int64_t intermediate;       /* multiple of 256 */
+    int r;                      /* LoRA rank: 8..64, multiple of 8 */
+    float lora_scale, eps;
+} qerl_decoder_dims;
+
+typedef struct qerl_chain qerl_chain;
+
+/* Workspace bytes of a chain of n_layers (0 if the dimensions are not covered). */
+size_t qerl_decoder_chain_ws_bytes(const qerl_decoder_dims *dims, int n_layers);
+
+/*
+ * Builds the chain's tables (jobs, tensor maps, buffers) in `ws` (caller
+ * owned, qerl_decoder_chain_ws_bytes bytes, 16-byte aligned) with blocking
+ * copies, and returns a host handle.  Call it outside stream capture; the
+ * pointers it is given (weights, x_in, x_out, attn, outputs) must stay valid
+ * while the handle is used.  x_in, x_out: bf16 [M, hidden] device.  After a
+ * run that reported an error, build the plan again (it resets the counters in
+ * ws).  Errors: QERL_ERR_INVALID_ARG, QERL_ERR_ALIGN, QERL_ERR_WORKSPACE,
+ * QERL_ERR_SHAPE, QERL_ERR_CUDA; nothing is launched on error.
+ */
+qerl_status qerl_decoder_chain_plan(const qerl_decoder_layer *layers, int n_layers,
+                                    const qerl_decoder_dims *dims, const void *x_in, void *x_out,
+                                    void *ws, size_t ws_bytes, qerl_chain **plan);
+
+/* Runs a planned chain on `stream` (one cooperative launch; capturable).  sigma,
+ * seed and step set the AQN noise of every norm; the chain's layer l is model
+ * layer first_layer + l, whose norms use noise keys 2 (first_layer + l) (before
+ * q/k/v) and 2 (first_layer + l) + 1 (before gate/up), so a model split over
+ * several chains draws the same noise as one chain.  Timeouts latch
+ * QERL_ERR_TIMEOUT (qerl_get_error). */
+qerl_status qerl_decoder_chain_run(const qerl_chain *plan, float sigma, uint64_t seed, uint64_t step,
+                                   uint32_t first_layer, qerl_stream_t stream);
+
+/* Frees the host handle (the workspace stays the caller's). */
+void qerl_decoder_chain_destroy(qerl_chain *plan);
+
 /* Scratch bytes an operation needs (0 if none).  Sizes as in the calls. */
 size_t qerl_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int r);
 

@@ -35,7 +35,8 @@ EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_lin
             "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
             "qerl_set_launch_chaining", "qerl_lora_linear_fwd_grouped_ws_bytes",
             "qerl_nvfp4_lora_linear_fwd_grouped",
-            "qerl_launch_count"]
+            "qerl_launch_count", "qerl_decoder_chain_ws_bytes", "qerl_decoder_chain_plan",
+            "qerl_decoder_chain_run", "qerl_decoder_chain_destroy"]
 
 
 class QerlError(RuntimeError):
@@ -91,6 +92,10 @@ def lib() -> C.CDLL:
             }
             sig["qerl_lora_linear_fwd_grouped_ws_bytes"] = ([i64, i64, i32, vp, i32], sz)
             sig["qerl_nvfp4_lora_linear_fwd_grouped"] = ([vp, i64, i64, i32, f32, vp, i32, i32, vp, sz, vp], i32)
+            sig["qerl_decoder_chain_ws_bytes"] = ([vp, i32], sz)
+            sig["qerl_decoder_chain_plan"] = ([vp, i32, vp, vp, vp, vp, sz, vp], i32)
+            sig["qerl_decoder_chain_run"] = ([vp, f32, u64, u64, u32, vp], i32)
+            sig["qerl_decoder_chain_destroy"] = ([vp], None)
             sig["qerl_nvfp4_lora_linear_fwd_packed"] = sig["qerl_nvfp4_lora_linear_fwd"]
             sig["qerl_nvfp4_lora_linear_bwd_packed"] = sig["qerl_nvfp4_lora_linear_bwd"]
             for name, (args, res) in sig.items():
@@ -309,3 +314,75 @@ def qerl_aqn_noise(H: int, seed: int, step: int, layer_id: int, want_raw: bool =
 
 def qerl_aqn_sigma(step: int, total_steps: int, sigma_start: float, sigma_end: float, num_stages: int) -> float:
     return lib().qerl_aqn_sigma(step, total_steps, sigma_start, sigma_end, num_stages)
+
+
+# ---------------------------------------------------------------- decoder chain
+class _LinW(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("tensor_scale", C.c_void_p), ("A", C.c_void_p),
+                ("B", C.c_void_p)]
+
+
+CHAIN_LINEARS = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+class _Layer(C.Structure):
+    _fields_ = [(n, _LinW) for n in CHAIN_LINEARS] + [
+        ("gamma_attn", C.c_void_p), ("gamma_mlp", C.c_void_p), ("attn", C.c_void_p), ("q_out", C.c_void_p),
+        ("k_out", C.c_void_p), ("v_out", C.c_void_p)]
+
+
+class _Dims(C.Structure):
+    _fields_ = [("M", C.c_int64), ("hidden", C.c_int64), ("q_dim", C.c_int64), ("kv_dim", C.c_int64),
+                ("intermediate", C.c_int64), ("r", C.c_int), ("lora_scale", C.c_float), ("eps", C.c_float)]
+
+
+def decoder_chain_ws_bytes(M, hidden, q_dim, kv_dim, intermediate, r, lora_scale, eps, n_layers) -> int:
+    d = _Dims(M, hidden, q_dim, kv_dim, intermediate, r, lora_scale, eps)
+    return lib().qerl_decoder_chain_ws_bytes(C.byref(d), n_layers)
+
+
+class DecoderChain:
+    """A planned chain of decoder layers (qerl_decoder_chain_plan / _run).
+
+    layers: one dict per layer with the seven linears under "q", "k", "v", "o",
+    "gate", "up", "down" as (packed codes, scales, tensor_scale, A, B), and
+    "gamma_attn", "gamma_mlp", "attn" (bf16 [M, hidden]) and optional "q_out",
+    "k_out", "v_out".  The tensors are kept referenced while the plan lives."""
+
+    def __init__(self, layers, M, hidden, q_dim, kv_dim, intermediate, r, lora_scale, eps, x_in, x_out, ws=None):
+        self._keep = [layers, x_in, x_out]
+        d = _Dims(M, hidden, q_dim, kv_dim, intermediate, r, lora_scale, eps)
+        n = lib().qerl_decoder_chain_ws_bytes(C.byref(d), len(layers))
+        if n == 0:
+            raise QerlError(2, "qerl_decoder_chain_ws_bytes")
+        self.ws = torch.empty(n, dtype=torch.uint8, device=x_in.device) if ws is None else ws
+        arr = (_Layer * len(layers))()
+        for i, Ly in enumerate(layers):
+            for nm in CHAIN_LINEARS:
+                codes, scales, ts, A, B = Ly[nm]
+                setattr(arr[i], nm, _LinW(_p(codes), _p(scales), _p(ts), _p(A), _p(B)))
+            arr[i].gamma_attn = _p(Ly["gamma_attn"])
+            arr[i].gamma_mlp = _p(Ly["gamma_mlp"])
+            arr[i].attn = _p(Ly["attn"])
+            arr[i].q_out = _p(Ly.get("q_out"))
+            arr[i].k_out = _p(Ly.get("k_out"))
+            arr[i].v_out = _p(Ly.get("v_out"))
+        h = C.c_void_p()
+        _check(lib().qerl_decoder_chain_plan(C.cast(arr, C.c_void_p), len(layers), C.byref(d), _p(x_in), _p(x_out),
+                                             _p(self.ws), self.ws.numel(), C.byref(h)), "qerl_decoder_chain_plan")
+        self._h = h
+
+    def run(self, sigma: float, seed: int, step: int, first_layer: int = 0, stream=None):
+        _check(lib().qerl_decoder_chain_run(self._h, float(sigma), seed, step, first_layer, _stream(stream)),
+               "qerl_decoder_chain_run")
+
+    def close(self):
+        if self._h:
+            lib().qerl_decoder_chain_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -33,6 +33,7 @@
 #include <mutex>
 #include <utility>
 
+#include "dequant.cuh"
 #include "linear.cuh"
 #include "sm100_ptx.cuh"
 
@@ -59,25 +60,22 @@ constexpr int FUSED_R = 32;  // LoRA rows loaded per k-step in fused mode
 template <int BN, bool FUSED = false>
 struct Cfg {
     // Dequant groups of four warps; group g takes the stages j = g (mod DQG).
-    // Decode tiles (short MMAs, HBM-bound) run three groups on half-size
-    // stages, so that more stages are being dequantized at once and each group
-    // finds a free stage; wide tiles keep two.
-    static constexpr int DQG = BN <= 64 ? 3 : 2;
+    static constexpr int DQG = 2;
     static constexpr int NUM_DQ_WARPS = DQG * DQ_GROUP_WARPS;
     static constexpr int WARP_RAW = NUM_DQ_WARPS, WARP_X = NUM_DQ_WARPS + 1, WARP_MMA = NUM_DQ_WARPS + 2;
     static constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
     // k-steps per pipeline stage (2 = 128 k, 4 = 256 k).
-    static constexpr int SPS = (BN >= 256 || BN <= 64) ? 2 : 4;
+    static constexpr int SPS = BN >= 256 ? 2 : 4;
     // A stage holds SPS k-steps of the dequantized weight tile (TMEM); at least
     // DQG of them, so a group never waits on a stage two mbarrier phases ahead
     // of the MMA (parity aliasing).  More stages than groups (where TMEM
     // allows): a group can fill a free stage while the MMA still reads the ones
     // filled before.
-    static constexpr int S = BN <= 64 ? 6 : (SPS == 4 ? 3 : 4);
+    static constexpr int S = SPS == 4 ? 3 : 4;
     static_assert(S >= DQG, "parity waits need at least one stage per dequant group");
     // Token-tile stages (smem), deeper than the A ring: a token slot is reloaded
     // only after the MMA that read it completed, a ~2 us round trip.
-    static constexpr int XS = BN <= 64 ? (FUSED ? 6 : 8) : (BN >= 128 ? 2 : 4);
+    static constexpr int XS = FUSED ? 3 : (BN >= 128 ? 2 : 4);
     static constexpr int R = 4;  // raw (code+scale) stages
     static_assert(GK % SPS == 0 && GK / SPS <= DQG, "each group has at most one stage per raw stage");
     static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
@@ -135,46 +133,6 @@ struct TcFwdParams {
     float lora_scale;    // fused: s
 };
 
-
-// bf16x2 {f, f} with f = e4m3(b) * 2^(126 - c), exact (<= 4 significant bits).
-// b20 holds the scale byte b in bits 20..27 (other bits are masked off here).
-// As FP32 bits that is e4m3(b) * 2^-120 for every byte < 0x80, subnormal
-// bytes included (they land on FP32 subnormals, which the multiply keeps), so
-// two exact multiplies by powers of two give f.
-__device__ __forceinline__ uint32_t scale_factor_bf16x2(uint32_t b20, float pow2)
-{
-    const float f = __uint_as_float(b20 & 0x0FF00000u) * pow2f(120) * pow2;
-    const uint32_t u = __float_as_uint(f);
-    return prmt(u, u, 0x3232u);  // {high half, high half}
-}
-
-// Eight E2M1 codes (one word, element 2j in the low nibble of byte j) -> four
-// bf16x2 words {elem 2j, elem 2j+1}.  The sign goes to bit 15 and the three
-// exponent/mantissa bits to bits 8..6, which as a bf16 is e2m1 * 2^-126 (the
-// code 0.5 becomes the subnormal 2^-127); one bf16x2 multiply by the block's
-// scale factor then gives e2m1 * e4m3 * 2^-c exactly.
-template <bool PACKED>
-__device__ __forceinline__ void dequant_word(uint32_t q, uint32_t f2, uint32_t *out)
-{
-    if (PACKED) {
-        // Packed layout: pair 0 already in place, pair 1 three bits low, pair 2
-        // six bits low with its signs at 13/29, pair 3 three bits high with its
-        // signs at 14/30.
-        out[0] = bf16x2_mul(q & 0x81C081C0u, f2);
-        out[1] = bf16x2_mul((q << 3) & 0x81C081C0u, f2);
-        out[2] = bf16x2_mul(((q << 6) & 0x01C001C0u) | ((q << 2) & 0x80008000u), f2);
-        out[3] = bf16x2_mul(((q >> 3) & 0x01C001C0u) | ((q << 1) & 0x80008000u), f2);
-        return;
-    }
-    const uint32_t q4 = q << 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        // byte 1 <- byte j of q4 (its high nibble is element 2j), byte 3 <- byte j of q
-        const uint32_t u = prmt(q4, q, 0x4400u + 0x1111u * (uint32_t)j);
-        const uint32_t raw = (u & 0x80008000u) | ((u >> 6) & 0x01C001C0u);
-        out[j] = bf16x2_mul(raw, f2);
-    }
-}
 
 // 16 columns of this warp's 32 TMEM lanes of the accumulator, as floats.
 __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])

@@ -259,6 +259,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Named barrier over `threads` threads that also ANDs a predicate across them:
+// every participant gets true only if all passed true.
+__device__ __forceinline__ bool named_bar_and(int id, int threads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
 
 }  // namespace ptx
 }  // namespace qerl
