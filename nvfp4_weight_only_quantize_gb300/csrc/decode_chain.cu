@@ -160,7 +160,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *bcast = abort_flag + 1;   // epilogue broadcast word
-    float *rs_s = reinterpret_cast<float *>(bars + 64);  // [64] per-token norm factors
+    float *rs_s = reinterpret_cast<float *>(bars + 64);   // [64] per-token norm factors
+    float *red_s = rs_s + BN;                             // [128] epilogue scratch
+    float *ns_s = red_s + EPI_THREADS;                    // [128] a tile's next-norm scale
+    volatile int *rs_phase = reinterpret_cast<volatile int *>(ns_s + TILE_N);  // phase whose input rs is in rs_s
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int jb = P.job_off[blockIdx.x], je = P.job_off[blockIdx.x + 1];
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(t_empty, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *rs_phase = -1;
         fence_mbar_init();
     }
     if (warp == WARP_MMA) {
@@ -291,14 +295,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 if (elect_one()) {
+                    // one copy each: the stage's four 64-k blocks of x and of the LoRA A rows
                     mbar_arrive_expect_tx(&x_full[slot], X_STAGE + C::AL_STAGE);
-#pragma unroll
-                    for (int sub = 0; sub < GK; ++sub) {
-                        const int kx = (kc * GK + sub) * BK;
-                        tma_load_2d_hint(X_ring + slot * X_STAGE + sub * X_STEP, &mp->x, &x_full[slot], kx, 0, pol);
-                        tma_load_2d_hint(AL_ring + slot * C::AL_STAGE + sub * C::AL_STEP, &mp->al, &x_full[slot], kx, 0,
-                                         pol);
-                    }
+                    tma_load_3d_hint(X_ring + slot * X_STAGE, &mp->x, &x_full[slot], 0, 0, kc * GK, pol);
+                    tma_load_3d_hint(AL_ring + slot * C::AL_STAGE, &mp->al, &x_full[slot], 0, 0, kc * GK, pol);
                 }
                 __syncwarp();
                 issued = j + 1;
@@ -484,44 +484,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else if (G.kind == GLUE_PRENORM) {
                     // tile J.tile of the first norm's input: xn = bf16(x * ns), sum of squares
-                    const int m = et >> 1, c0 = J.tile * TILE_N + (et & 1) * 64;
-                    float ss = 0.0f;
-                    if (m < P.M) {
-                        for (int c = c0; c < c0 + 64; c += 8) {
-                            const uint4 xv = *reinterpret_cast<const uint4 *>(G.a + (size_t)m * G.width + c);
-                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                            uint32_t o[4];
+                    ns_s[et] = G.ns[J.tile * TILE_N + et];
+                    named_bar_sync(BAR_EPI, EPI_THREADS);
+                    const int m = et >> 1, cb = (et & 1) * 64;
+                    const __nv_bfloat16 *xr = G.a + (size_t)m * G.width + J.tile * TILE_N + cb;
+                    uint4 xv[8];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float a0 = bf16lo(xw[e]), a1 = bf16hi(xw[e]);
-                                ss = fmaf(a0, a0, ss);
-                                ss = fmaf(a1, a1, ss);
-                                const __nv_bfloat162 p2 =
-                                    __floats2bfloat162_rn(a0 * G.ns[c + 2 * e], a1 * G.ns[c + 2 * e + 1]);
-                                o[e] = *reinterpret_cast<const uint32_t *>(&p2);
-                            }
-                            *reinterpret_cast<uint4 *>(G.out + (size_t)m * G.width + c) = make_uint4(o[0], o[1], o[2], o[3]);
+                    for (int c = 0; c < 8; ++c)  // every load in flight before the math
+                        xv[c] = m < P.M ? *reinterpret_cast<const uint4 *>(xr + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+                    float ss = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t xw[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float a0 = bf16lo(xw[e]), a1 = bf16hi(xw[e]);
+                            ss = fmaf(a0, a0, ss);
+                            ss = fmaf(a1, a1, ss);
+                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(a0 * ns_s[cb + 8 * c + 2 * e],
+                                                                            a1 * ns_s[cb + 8 * c + 2 * e + 1]);
+                            o[e] = *reinterpret_cast<const uint32_t *>(&p2);
                         }
+                        if (m < P.M)
+                            *reinterpret_cast<uint4 *>(G.out + (size_t)m * G.width + J.tile * TILE_N + cb + 8 * c) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
                     }
                     ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
                     if ((et & 1) == 0) G.sq[J.tile * BN + m] = ss;
                 } else {
                     // SwiGLU over columns [unit * cols, +cols)
                     const int c0 = J.tile * G.cols, c1 = min(G.width, c0 + G.cols);
-                    const int vecs = (c1 - c0) / 8;
-                    for (int it = et; it < P.M * vecs; it += EPI_THREADS) {
-                        const int m = it / vecs, c = c0 + (it % vecs) * 8;
-                        const uint4 gv = *reinterpret_cast<const uint4 *>(G.a + (size_t)m * G.width + c);
-                        const uint4 uv = *reinterpret_cast<const uint4 *>(G.b + (size_t)m * G.width + c);
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
-                        uint32_t o[4];
+                    const int vecs = (c1 - c0) / 8, items = P.M * vecs;
+                    for (int it0 = et; it0 < items; it0 += 4 * EPI_THREADS) {
+                        uint4 gv[4], uv[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(silu(bf16lo(gw[e])) * bf16lo(uw[e]),
-                                                                            silu(bf16hi(gw[e])) * bf16hi(uw[e]));
-                            o[e] = *reinterpret_cast<const uint32_t *>(&p2);
+                        for (int b = 0; b < 4; ++b) {  // four items' loads in flight at once
+                            const int it = it0 + b * EPI_THREADS;
+                            const int m = it / vecs, c = c0 + (it % vecs) * 8;
+                            gv[b] = it < items ? *reinterpret_cast<const uint4 *>(G.a + (size_t)m * G.width + c)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+                            uv[b] = it < items ? *reinterpret_cast<const uint4 *>(G.b + (size_t)m * G.width + c)
+                                               : make_uint4(0u, 0u, 0u, 0u);
                         }
-                        *reinterpret_cast<uint4 *>(G.out + (size_t)m * G.width + c) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const int it = it0 + b * EPI_THREADS;
+                            if (it >= items) break;
+                            const int m = it / vecs, c = c0 + (it % vecs) * 8;
+                            const uint32_t gw[4] = {gv[b].x, gv[b].y, gv[b].z, gv[b].w};
+                            const uint32_t uw[4] = {uv[b].x, uv[b].y, uv[b].z, uv[b].w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 p2 = __floats2bfloat162_rn(silu(bf16lo(gw[e])) * bf16lo(uw[e]),
+                                                                                silu(bf16hi(gw[e])) * bf16hi(uw[e]));
+                                o[e] = *reinterpret_cast<const uint32_t *>(&p2);
+                            }
+                            *reinterpret_cast<uint4 *>(G.out + (size_t)m * G.width + c) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
                     }
                 }
                 __threadfence();
@@ -533,7 +554,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
             // ----------------------------------- matmul job
             const Lin &L = P.lins[J.idx];
+            if (L.kind == LIN_NORMED && *rs_phase != L.phase) {
+                // rs = rsqrt(mean h^2 + eps) of the linear's (normed) input, once per
+                // input: the partial sums are final once the phase before has completed
+                if (et == 0) *bcast = wait_phase(L.phase - 1) ? 1 : 0;
+                named_bar_sync(BAR_EPI, EPI_THREADS);
+                ok = *bcast != 0;
+                if (!ok) break;
+                const int m = et & (BN - 1), hf = et / BN;  // token, half of the tiles
+                float ss = 0.0f;
+                for (int i0 = hf * 16; i0 < L.sq_tiles; i0 += 32) {
+                    float sv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sv[e] = i0 + e < L.sq_tiles ? L.sq_in[(i0 + e) * BN + m] : 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ss += sv[e];
+                }
+                red_s[et] = ss;
+                named_bar_sync(BAR_EPI, EPI_THREADS);
+                if (et < BN) rs_s[et] = rsqrtf((red_s[et] + red_s[et + BN]) / (float)L.K + P.eps);
+                if (et == 0) *rs_phase = L.phase;
+                named_bar_sync(BAR_EPI, EPI_THREADS);
+            }
             const int nmain = J.kc1 - J.kc0;
+
             const int jl = j + nmain;  // the job's LoRA stage
             j = jl + 1;
             const float st = *L.ts;
@@ -629,12 +673,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int n0 = J.tile * TILE_N;
             __nv_bfloat16 *Y = reinterpret_cast<__nv_bfloat16 *>(Ystage);
             if (L.kind == LIN_NORMED) {
-                if (et < BN) {
-                    float ss = 0.0f;
-                    for (int i = 0; i < L.sq_tiles; ++i) ss += L.sq_in[i * BN + et];
-                    rs_s[et] = rsqrtf(ss / (float)L.K + P.eps);
-                }
-                named_bar_sync(BAR_EPI, EPI_THREADS);
 #pragma unroll
                 for (int m = 0; m < BN; ++m) Y[m * TILE_N + row] = __float2bfloat16_rn(v[m] * ysc * rs_s[m]);
                 named_bar_sync(BAR_EPI, EPI_THREADS);
@@ -649,13 +687,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // h_out = bf16(h_in + bf16(v)), xn = bf16(h_out * ns), sum of squares of h_out
 #pragma unroll
                 for (int m = 0; m < BN; ++m) Y[m * TILE_N + row] = __float2bfloat16_rn(v[m] * ysc);
+                if (L.xn_out) ns_s[et] = L.ns_next[n0 + et];
                 named_bar_sync(BAR_EPI, EPI_THREADS);
                 const int m = et >> 1, cb = (et & 1) * 64;
                 float ss = 0.0f;
                 if (m < P.M) {
-                    for (int c = cb; c < cb + 64; c += 8) {
+                    uint4 hin[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)  // every load in flight before the math
+                        hin[c] = *reinterpret_cast<const uint4 *>(L.h_in + (size_t)m * L.N + n0 + cb + 8 * c);
+#pragma unroll
+                    for (int ci = 0; ci < 8; ++ci) {
+                        const int c = cb + 8 * ci;
                         const uint4 yv = *reinterpret_cast<const uint4 *>(Y + m * TILE_N + c);
-                        const uint4 hv = *reinterpret_cast<const uint4 *>(L.h_in + (size_t)m * L.N + n0 + c);
+                        const uint4 hv = hin[ci];
                         const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w}, hw[4] = {hv.x, hv.y, hv.z, hv.w};
                         uint32_t ho[4], xo[4];
 #pragma unroll
@@ -667,8 +712,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ss = fmaf(a0, a0, ss);
                             ss = fmaf(a1, a1, ss);
                             if (L.xn_out) {
-                                const __nv_bfloat162 x2 = __floats2bfloat162_rn(a0 * L.ns_next[n0 + c + 2 * e],
-                                                                                a1 * L.ns_next[n0 + c + 2 * e + 1]);
+                                const __nv_bfloat162 x2 =
+                                    __floats2bfloat162_rn(a0 * ns_s[c + 2 * e], a1 * ns_s[c + 2 * e + 1]);
                                 xo[e] = *reinterpret_cast<const uint32_t *>(&x2);
                             }
                         }
@@ -959,10 +1004,7 @@ extern "C" qerl_status qerl_decoder_chain_plan(const qerl_decoder_layer *layers,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map_2d(&mp.scl, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.scales, K / 16, N, K / 16, KC / 16, TILE_N,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !make_map_2d(&mp.al, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.A, K, r, (uint64_t)K * 2, BK, RL,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map_2d(&mp.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xin, K, M, (uint64_t)K * 2, BK, BN,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+            !make_map_kblocks(&mp.al, w.A, K, r, RL, GK) || !make_map_kblocks(&mp.x, xin, K, M, BN, GK))
             return false;
         lins.push_back(Lr);
         maps.push_back(mp);

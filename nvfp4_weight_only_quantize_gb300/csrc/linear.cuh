@@ -53,6 +53,12 @@ inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 // rows of `row_bytes`; false if the driver rejects it.
 bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+// 3-D TMA map of a bf16 [rows, K] row-major matrix (K % 64 == 0) whose box is
+// box_rows rows x kblocks consecutive 64-element k-blocks, written to shared
+// memory as kblocks tiles [box_rows][64] in the 128-byte swizzle (the layout of
+// kblocks separate 2-D boxes, in one copy).  Coordinates: (0, row, k / 64).
+bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows,
+                      uint32_t kblocks);
 
 // Rank products on tensor cores (rank_tc.cu), split over the reduction: for g < G,
 //   part_g[z][m][j] = sum over k in split z of X[m, k] * W_g[j, k],  j < r_g,

@@ -844,6 +844,22 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_kblocks(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows,
+                      uint32_t kblocks)
+{
+    auto fn = encode_fn();
+    if (!fn || K % 64 != 0) return false;
+    // bf16 [rows, K] viewed as (64 k, row, k-block): one box = box_rows rows of
+    // kblocks consecutive 64-element k-blocks, landing as kblocks [row][64] tiles
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, kblocks};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {
     return tc_fwd_applies(M, N, K, r) ? plan_fwd(M, &N, 1, K, r).total : 0;
