@@ -391,7 +391,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t tcol = trow + (uint32_t)(A_COL0 + s * 32 * GK);
                     if (main_stage) {
-                        // every code and scale of the row first, then the raw slot goes back
+                        // every code and scale of the row first (all loads in flight); the raw
+                        // slot goes back once every loaded word has been used
                         const uint8_t *rb = R_ring + rs * RAW_STAGE;
                         uint4 cw[2 * GK];
 #pragma unroll
@@ -401,8 +402,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 *reinterpret_cast<const uint4 *>(rb + row * 128 + (((2 * sub + 1) ^ (row & 7)) * 16));
                         }
                         const uint4 scv = *reinterpret_cast<const uint4 *>(rb + RAW_CODES + row * 16);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&raw_empty[rs]);
                         const uint32_t scw[GK] = {scv.x, scv.y, scv.z, scv.w};
 #pragma unroll
                         for (int sub = 0; sub < GK; ++sub) {
@@ -423,6 +422,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             dequant_word<PACKED>(c1.w, f3, out + 28);
                             tmem_st32(tcol + (uint32_t)(sub * 32), out);
                         }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&raw_empty[rs]);
                     } else {
                         // LoRA up-projection rows B[n, 0..63], zero past r (r % 8 == 0)
                         uint32_t out[32];

@@ -442,8 +442,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
             if (main_stage && !__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(g / C::R) & 1u))) break;
             const int nsub = min(SPS, n_steps - j * SPS);
             // A main stage reads all of its codes and scales first (every load in
-            // flight at once), then hands the raw slot back to the producer
-            // before dequantizing from registers.
+            // flight at once); the raw slot goes back to the producer once the
+            // stage's dequantized values are written (every loaded word used).
             uint4 cw[2 * SPS];
             uint32_t scw[SPS];
             if (main_stage) {
@@ -459,8 +459,6 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                         *reinterpret_cast<const uint4 *>(rb + row * 128 + (((2 * q + 1) ^ (row & 7)) * 16));
                     scw[sub] = *reinterpret_cast<const uint32_t *>(rb + RAW_CODES + row * 16 + q * 4);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[rs]);
             }
 #pragma unroll
             for (int sub = 0; sub < SPS; ++sub) {
@@ -509,6 +507,10 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                 }
                 // row `row` of the step's A tile: TMEM lane `row`, 32 columns of bf16 pairs
                 tmem_st32(trow + (uint32_t)(C::A_COL0 + s * 32 * SPS + sub * 32), out);
+            }
+            if (main_stage) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);
             }
             tmem_wait_st();
             tc_fence_before();

@@ -46,7 +46,7 @@ def build(force: bool = False) -> str:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call([
             "gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
-            "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"])
+            "-fno-fast-math", "-fopenmp", "-Wall", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -71,6 +71,8 @@ def lib():
             L.orc_lora_linear_fwd.argtypes = [_u16, i64, i64, i64, _u8, _u8, f32, _u16, _u16,
                                               i32, f64, _i64, i64, _f64, C.c_void_p]
             L.orc_lora_linear_fwd.restype = None
+            L.orc_set_threads.argtypes = [i32]
+            L.orc_set_threads.restype = None
             L.orc_lora_linear_bwd.argtypes = [_u16, _u16, i64, i64, i64, _u8, _u8, f32, _u16,
                                               _u16, i32, f64,
                                               C.c_void_p, i64, C.c_void_p,
@@ -140,6 +142,11 @@ def nvfp4_dequantize(codes, scales, tensor_scale, N, K) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- linear
+def set_threads(n: int):
+    """Threads the linear forward may use (1, the default: single-threaded)."""
+    lib().orc_set_threads(int(n))
+
+
 def lora_linear_fwd(x_bits, codes, scales, tensor_scale, A_bits, B_bits, lora_scale,
                     rows=None, want_t=False):
     """y = x W_hat^T + s (x A^T) B^T in fp64 for the token rows ``rows``."""

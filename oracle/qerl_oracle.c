@@ -1,8 +1,10 @@
 /*
  * qerl_oracle.c -- TEST INFRASTRUCTURE ONLY.
  *
- * A plain, slow, single-threaded CPU restatement of what the NVFP4 weight-only
- * LoRA linear path computes, used to check the CUDA library.  Only the test
+ * A plain, slow CPU restatement of what the NVFP4 weight-only LoRA linear path
+ * computes, used to check the CUDA library.  Single-threaded unless
+ * orc_set_threads asks for more: the linear forward then hands whole output
+ * features to threads (OpenMP), each element computed exactly as alone.  Only the test
  * suite, the smoke check and the benchmark's CPU-baseline leg may load it.  It
  * shares no code, header, table or constant generator with the CUDA library.
  *
@@ -255,6 +257,10 @@ void orc_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales,
  * x bf16 [M, K]; A bf16 [r, K]; B bf16 [N, r].  Only the nrows token rows listed
  * in rows[] are computed; y is [nrows, N] and t (optional) is [nrows, r] holding
  * x * A^T for those rows. */
+/* Threads the linear forward may use (1 = single-threaded, the default). */
+static int g_threads = 1;
+void orc_set_threads(int n) { g_threads = n > 0 ? n : 1; }
+
 void orc_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N,
                          const uint8_t *codes, const uint8_t *scales,
                          float tensor_scale, const uint16_t *A,
@@ -264,7 +270,6 @@ void orc_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N,
 {
     int64_t i, n, k;
     int j;
-    double *wrow = (double *)malloc((size_t)K * sizeof(double));
     double *tt = (double *)calloc((size_t)(nrows * (r > 0 ? r : 1)), sizeof(double));
     (void)M;
 
@@ -277,21 +282,31 @@ void orc_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N,
             tt[i * r + j] = acc;
         }
 
-    for (n = 0; n < N; ++n) {
-        for (k = 0; k < K; ++k)
-            wrow[k] = w_hat(codes, scales, (double)tensor_scale, K, n, k);
-        for (i = 0; i < nrows; ++i) {
-            double acc = 0.0, lora = 0.0;
-            for (k = 0; k < K; ++k)
-                acc += orc_bf16_value(x[rows[i] * K + k]) * wrow[k];
-            for (j = 0; j < r; ++j)
-                lora += tt[i * r + j] * orc_bf16_value(B[n * r + j]);
-            y[i * N + n] = acc + lora_scale * lora;
+    /* Output features are independent: with threads, each takes whole features
+     * (its own dequantized row), the sums over k run in the same order. */
+#pragma omp parallel num_threads(g_threads) if (g_threads > 1)
+    {
+        double *wrow = (double *)malloc((size_t)K * sizeof(double));
+        int64_t nn, ii, kk;
+        int jj;
+#pragma omp for schedule(static)
+        for (nn = 0; nn < N; ++nn) {
+            for (kk = 0; kk < K; ++kk)
+                wrow[kk] = w_hat(codes, scales, (double)tensor_scale, K, nn, kk);
+            for (ii = 0; ii < nrows; ++ii) {
+                double acc = 0.0, lora = 0.0;
+                for (kk = 0; kk < K; ++kk)
+                    acc += orc_bf16_value(x[rows[ii] * K + kk]) * wrow[kk];
+                for (jj = 0; jj < r; ++jj)
+                    lora += tt[ii * r + jj] * orc_bf16_value(B[nn * r + jj]);
+                y[ii * N + nn] = acc + lora_scale * lora;
+            }
         }
+        free(wrow);
     }
+    (void)n;
     if (t)
         memcpy(t, tt, (size_t)(nrows * r) * sizeof(double));
-    free(wrow);
     free(tt);
 }
 

@@ -101,3 +101,24 @@ def test_backward_subsets_match_full():
     np.testing.assert_array_equal(sub[0], full[0][rows])
     np.testing.assert_array_equal(sub[1], full[1][:, cols])
     np.testing.assert_array_equal(sub[2], full[2][nrows])
+
+
+def test_threaded_forward_equals_single_threaded():
+    """Threads take whole output features; every element is summed in the same
+    order, so the threaded forward equals the single-threaded one bit for bit."""
+    rng = np.random.default_rng(5)
+    N, K, M, r = 96, 64, 3, 4
+    W = synth.bits(synth.weight(N, K, 71))
+    rc, codes, scales, st = oracle.nvfp4_quantize(W)
+    assert rc == 0
+    x = synth.bits(synth.activations(M, K, 72))
+    A = synth.bits(synth.lora_A(r, K, 73))
+    B = synth.bits(synth.lora_B(N, r, 74))
+    y1, t1 = oracle.lora_linear_fwd(x, codes, scales, st, A, B, 2.0, want_t=True)
+    try:
+        oracle.set_threads(4)
+        y4, t4 = oracle.lora_linear_fwd(x, codes, scales, st, A, B, 2.0, want_t=True)
+    finally:
+        oracle.set_threads(1)
+    assert np.array_equal(y1, y4) and np.array_equal(t1, t4)
+    del rng
