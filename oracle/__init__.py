@@ -73,6 +73,17 @@ def lib():
             L.orc_lora_linear_fwd.restype = None
             L.orc_set_threads.argtypes = [i32]
             L.orc_set_threads.restype = None
+            L.orc_e8m0_value.argtypes = [u8]; L.orc_e8m0_value.restype = f64
+            L.orc_mxfp4_quantize.argtypes = [_u16, i64, i64, i64, _u8, _u8]
+            L.orc_mxfp4_quantize.restype = i32
+            L.orc_mxfp4_dequantize.argtypes = [_u8, _u8, i64, i64, _f64]
+            L.orc_mxfp4_dequantize.restype = None
+            L.orc_lora_linear_fwd_f32ab.argtypes = [_u16, i64, i64, i64, _u8, _u8, f32, _f32, _f32,
+                                                    i32, f64, _i64, i64, _f64, C.c_void_p]
+            L.orc_lora_linear_fwd_f32ab.restype = None
+            L.orc_mxfp4_lora_linear_fwd.argtypes = [_u16, i64, i64, i64, _u8, _u8, _u16, _u16,
+                                                    i32, f64, _i64, i64, _f64, C.c_void_p]
+            L.orc_mxfp4_lora_linear_fwd.restype = None
             L.orc_lora_linear_bwd.argtypes = [_u16, _u16, i64, i64, i64, _u8, _u8, f32, _u16,
                                               _u16, i32, f64,
                                               C.c_void_p, i64, C.c_void_p,
@@ -160,6 +171,58 @@ def lora_linear_fwd(x_bits, codes, scales, tensor_scale, A_bits, B_bits, lora_sc
     lib().orc_lora_linear_fwd(x_bits, M, K, N, _c(codes, np.uint8), _c(scales, np.uint8),
                               float(tensor_scale), _c(A_bits, np.uint16), _c(B_bits, np.uint16),
                               r, float(lora_scale), rows, len(rows), y, _ptr(t))
+    return (y, t) if want_t else y
+
+
+def lora_linear_fwd_f32ab(x_bits, codes, scales, tensor_scale, A_f32, B_f32, lora_scale, rows=None,
+                          want_t=False):
+    """The forward with FP32 LoRA adapters (A [r,K], B [N,r] float32)."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    N = codes.shape[0]
+    r = A_f32.shape[0]
+    rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    y = np.zeros((len(rows), N), np.float64)
+    t = np.zeros((len(rows), r), np.float64) if want_t else None
+    lib().orc_lora_linear_fwd_f32ab(x_bits, M, K, N, _c(codes, np.uint8), _c(scales, np.uint8),
+                                    float(tensor_scale), _c(A_f32, np.float32), _c(B_f32, np.float32),
+                                    r, float(lora_scale), rows, len(rows), y, _ptr(t))
+    return (y, t) if want_t else y
+
+
+# ---------------------------------------------------------------- MXFP4
+def e8m0_value(b: int) -> float:
+    return lib().orc_e8m0_value(b)
+
+
+def mxfp4_quantize(W_bits: np.ndarray):
+    """W_bits uint16 [N, K] -> (status, codes u8 [N,K/2], E8M0 scales u8 [N,K/32])."""
+    W_bits = _c(W_bits, np.uint16)
+    N, K = W_bits.shape
+    codes = np.zeros((N, max(K // 2, 0)), np.uint8)
+    scales = np.zeros((N, max(K // 32, 0)), np.uint8)
+    rc = lib().orc_mxfp4_quantize(W_bits, N, K, K, codes, scales)
+    return rc, codes, scales
+
+
+def mxfp4_dequantize(codes, scales, N, K) -> np.ndarray:
+    out = np.zeros((N, K), np.float64)
+    lib().orc_mxfp4_dequantize(_c(codes, np.uint8), _c(scales, np.uint8), N, K, out)
+    return out
+
+
+def mxfp4_lora_linear_fwd(x_bits, codes, scales, A_bits, B_bits, lora_scale, rows=None, want_t=False):
+    """y = x W_hat^T + s (x A^T) B^T with an MXFP4 weight, fp64."""
+    x_bits = _c(x_bits, np.uint16)
+    M, K = x_bits.shape
+    N = codes.shape[0]
+    r = A_bits.shape[0]
+    rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    y = np.zeros((len(rows), N), np.float64)
+    t = np.zeros((len(rows), r), np.float64) if want_t else None
+    lib().orc_mxfp4_lora_linear_fwd(x_bits, M, K, N, _c(codes, np.uint8), _c(scales, np.uint8),
+                                    _c(A_bits, np.uint16), _c(B_bits, np.uint16), r, float(lora_scale),
+                                    rows, len(rows), y, _ptr(t))
     return (y, t) if want_t else y
 
 

@@ -15,7 +15,11 @@
  *           FP32 tensor-wise scale; the cuDNN block-scaling recipe: block scale
  *           = quantize_round_up(amax(vals)/vmax), value = round_to_even(v/scale).
  *  [LoRA]   same page, LoRA paragraph: frozen W plus a trainable low-rank update
- *           kept in higher precision.
+ *           kept in higher precision (e.g. FP16 or FP32).
+ *  [MX]     same page, "NVFP4" section: NVFP4 against MXFP4, whose blocks are 32
+ *           values with a power-of-two (E8M0) scale.  The block-scale rule is
+ *           the OCP Microscaling (MX) v1.0 one: shared exponent =
+ *           floor(log2(amax)) - emax of the element type (2 for E2M1).
  *  [Impl]   same page, "Implementation and Practical Details": weight-only
  *           quantization; activations and gradients stay in high precision.
  *  [AQN-S]  "QeRL: Beyond Efficiency -- Quantization-enhanced Reinforcement
@@ -240,6 +244,65 @@ static double w_hat(const uint8_t *codes, const uint8_t *scales, double s_t,
 }
 
 /* Dequantize rows [0, N) into out [N, K] (fp64). */
+/* E8M0 scale byte [MX]: 2^(b - 127); 0xFF is NaN (never emitted). */
+double orc_e8m0_value(uint8_t b) { return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127); }
+
+/* MXFP4 quantizer [MX]: per block of 32 consecutive k, e = floor(log2(amax_b))
+ * - 2 clamped to [-127, 127] (all-zero block: e = -127), scale byte e + 127,
+ * element code = E2M1 nearest value of w * 2^-e (ties to the even code,
+ * saturating at 6, zero as code 0).  Codes pack as for NVFP4; scales are a
+ * row-major [N, K/32] byte array.  No tensor scale. */
+int orc_mxfp4_quantize(const uint16_t *W, int64_t N, int64_t K, int64_t ldw,
+                       uint8_t *codes, uint8_t *scales)
+{
+    int64_t n, k, b;
+    if (K % 32 != 0 || N < 0 || ldw < K)
+        return ORC_ERR_SHAPE;
+    for (n = 0; n < N; ++n)
+        for (k = 0; k < K; ++k)
+            if (!isfinite(bf16_bits_to_float(W[n * ldw + k])))
+                return ORC_ERR_NONFINITE;
+    memset(codes, 0, (size_t)(N * (K / 2)));
+    for (n = 0; n < N; ++n)
+        for (b = 0; b < K / 32; ++b) {
+            const uint16_t *blk = W + n * ldw + b * 32;
+            float amax = 0.0f;
+            int i, e = -127, ex;
+            for (i = 0; i < 32; ++i) {
+                float a = fabsf(bf16_bits_to_float(blk[i]));
+                if (a > amax)
+                    amax = a;
+            }
+            if (amax > 0.0f) {
+                frexpf(amax, &ex); /* amax = m 2^ex, m in [0.5, 1): floor(log2) = ex - 1 */
+                e = ex - 1 - 2;
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            scales[n * (K / 32) + b] = (uint8_t)(e + 127);
+            for (i = 0; i < 32; ++i) {
+                int64_t kk = b * 32 + i;
+                uint8_t c = orc_e2m1_round(ldexpf(bf16_bits_to_float(blk[i]), -e));
+                if (kk % 2 == 0)
+                    codes[n * (K / 2) + kk / 2] |= c;
+                else
+                    codes[n * (K / 2) + kk / 2] |= (uint8_t)(c << 4);
+            }
+        }
+    return ORC_OK;
+}
+
+/* w_hat = e2m1(code) * 2^(scale byte - 127) of an MXFP4 weight, fp64 [N, K]. */
+void orc_mxfp4_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t N, int64_t K, double *out)
+{
+    int64_t n, k;
+    for (n = 0; n < N; ++n)
+        for (k = 0; k < K; ++k)
+            out[n * K + k] = orc_e2m1_value(code_at(codes, K, n, k)) * orc_e8m0_value(scales[n * (K / 32) + k / 32]);
+}
+
 void orc_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales,
                           float tensor_scale, int64_t N, int64_t K, double *out)
 {
@@ -261,24 +324,36 @@ void orc_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales,
 static int g_threads = 1;
 void orc_set_threads(int n) { g_threads = n > 0 ? n : 1; }
 
-void orc_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N,
-                         const uint8_t *codes, const uint8_t *scales,
-                         float tensor_scale, const uint16_t *A,
-                         const uint16_t *B, int r, double lora_scale,
-                         const int64_t *rows, int64_t nrows, double *y,
-                         double *t)
+/* A weight element of format fmt (0: NVFP4 with tensor scale s_t; 1: MXFP4). */
+static double weight_value(int fmt, const uint8_t *codes, const uint8_t *scales, double s_t, int64_t K,
+                           int64_t n, int64_t k)
 {
-    int64_t i, n, k;
+    if (fmt == 1)
+        return orc_e2m1_value(code_at(codes, K, n, k)) * orc_e8m0_value(scales[n * (K / 32) + k / 32]);
+    return w_hat(codes, scales, s_t, K, n, k);
+}
+/* An adapter element: bf16 bit patterns, or FP32 values when f32. */
+static double adapter_value(const void *p, int f32, int64_t i)
+{
+    return f32 ? (double)((const float *)p)[i] : orc_bf16_value(((const uint16_t *)p)[i]);
+}
+
+/* y[i, n] = sum_k x[rows[i], k] w_hat[n, k] + s * sum_j t[i, j] B[n, j],
+ * t[i, j] = sum_k x[rows[i], k] A[j, k], in fp64 [LoRA][Impl]. */
+static void lora_fwd(int fmt, int f32_adapters, const uint16_t *x, int64_t K, int64_t N, const uint8_t *codes,
+                     const uint8_t *scales, float tensor_scale, const void *A, const void *B, int r,
+                     double lora_scale, const int64_t *rows, int64_t nrows, double *y, double *t)
+{
+    int64_t i, k;
     int j;
     double *tt = (double *)calloc((size_t)(nrows * (r > 0 ? r : 1)), sizeof(double));
-    (void)M;
 
     /* t = x * A^T for the selected rows. */
     for (i = 0; i < nrows; ++i)
         for (j = 0; j < r; ++j) {
             double acc = 0.0;
             for (k = 0; k < K; ++k)
-                acc += orc_bf16_value(x[rows[i] * K + k]) * orc_bf16_value(A[(int64_t)j * K + k]);
+                acc += orc_bf16_value(x[rows[i] * K + k]) * adapter_value(A, f32_adapters, (int64_t)j * K + k);
             tt[i * r + j] = acc;
         }
 
@@ -292,22 +367,47 @@ void orc_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N,
 #pragma omp for schedule(static)
         for (nn = 0; nn < N; ++nn) {
             for (kk = 0; kk < K; ++kk)
-                wrow[kk] = w_hat(codes, scales, (double)tensor_scale, K, nn, kk);
+                wrow[kk] = weight_value(fmt, codes, scales, (double)tensor_scale, K, nn, kk);
             for (ii = 0; ii < nrows; ++ii) {
                 double acc = 0.0, lora = 0.0;
                 for (kk = 0; kk < K; ++kk)
                     acc += orc_bf16_value(x[rows[ii] * K + kk]) * wrow[kk];
                 for (jj = 0; jj < r; ++jj)
-                    lora += tt[ii * r + jj] * orc_bf16_value(B[nn * r + jj]);
+                    lora += tt[ii * r + jj] * adapter_value(B, f32_adapters, nn * r + jj);
                 y[ii * N + nn] = acc + lora_scale * lora;
             }
         }
         free(wrow);
     }
-    (void)n;
     if (t)
         memcpy(t, tt, (size_t)(nrows * r) * sizeof(double));
     free(tt);
+}
+
+void orc_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
+                         const uint8_t *scales, float tensor_scale, const uint16_t *A, const uint16_t *B, int r,
+                         double lora_scale, const int64_t *rows, int64_t nrows, double *y, double *t)
+{
+    (void)M;
+    lora_fwd(0, 0, x, K, N, codes, scales, tensor_scale, A, B, r, lora_scale, rows, nrows, y, t);
+}
+
+/* The forward with FP32 LoRA adapters A [r, K] and B [N, r] [LoRA]. */
+void orc_lora_linear_fwd_f32ab(const uint16_t *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
+                               const uint8_t *scales, float tensor_scale, const float *A, const float *B, int r,
+                               double lora_scale, const int64_t *rows, int64_t nrows, double *y, double *t)
+{
+    (void)M;
+    lora_fwd(0, 1, x, K, N, codes, scales, tensor_scale, A, B, r, lora_scale, rows, nrows, y, t);
+}
+
+/* The forward with an MXFP4 weight (codes, E8M0 scales [N, K/32]) [MX]. */
+void orc_mxfp4_lora_linear_fwd(const uint16_t *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
+                               const uint8_t *scales, const uint16_t *A, const uint16_t *B, int r, double lora_scale,
+                               const int64_t *rows, int64_t nrows, double *y, double *t)
+{
+    (void)M;
+    lora_fwd(1, 0, x, K, N, codes, scales, 1.0f, A, B, r, lora_scale, rows, nrows, y, t);
 }
 
 /* Backward with W_hat frozen [LoRA][Impl]:
