@@ -280,6 +280,8 @@ qerl_status qerl_nvfp4_lora_linear_bwd_packed(const void *dy, const void *x, int
  *   tokens: Philox4x64-10 with key (seed, layer_id), counter (c/4, step, 0, 0),
  *   Box-Muller on word pairs (see qerl_aqn_noise).  sigma == 0 is plain RMSNorm.
  *   ws (device) >= qerl_workspace_bytes(QERL_OP_AQN_RMSNORM, M, 0, H, 0).
+ *   One launch for H <= 16384 (each CTA draws the noisy scale into shared
+ *   memory); wider rows draw it into ws first.
  */
 qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
                              float sigma, uint64_t seed, uint64_t step, uint32_t layer_id,
@@ -292,6 +294,8 @@ qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *ga
  * key (seed, layer_id)); z[4i], z[4i+1] from (w0, w1) and z[4i+2], z[4i+3]
  * from (w2, w3) with u1 = ((wa >> 11) + 1) * 2^-53, u2 = (wb >> 11) * 2^-53,
  * z = sqrt(-2 ln u1) * (cos 2 pi u2, sin 2 pi u2); raw_out[c] = w_(c mod 4).
+ * Computed in FP32 (ln u1 as log1p(u1 - 1) near 1); within a few 1e-6 of the
+ * exact values.
  */
 qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, uint32_t layer_id,
                            float *z_out, uint64_t *raw_out, qerl_stream_t stream);
@@ -307,6 +311,42 @@ float qerl_aqn_sigma(int64_t step, int64_t total_steps, float sigma_start, float
                      int num_stages);
 
 /*
+ * Format variants (bitsofall "QeRL: NVFP4-Quantized Reinforcement Learning",
+ * "NVFP4" section, which sets NVFP4 against MXFP4, whose blocks are 32 values
+ * with a power-of-two scale; and its LoRA paragraph, which keeps the adapters
+ * in higher precision, e.g. FP32).  These run on CUDA cores.
+ *
+ * MXFP4 quantizer: W (device) bf16 [N, K] (row stride ldw elements), K % 32 ==
+ * 0 -> codes (device, 16-byte aligned) u8 [N, K/2] (element 2j in the low
+ * nibble of byte j, E2M1 codes as for NVFP4) and scales (device) u8 [N, K/32]
+ * E8M0 bytes: for each block of 32, e = floor(log2(amax)) - 2 (the OCP MX
+ * rule: 2 is the exponent of E2M1's largest value 6 = 1.5 * 2^2) clamped to
+ * [-127, 127] (-127 for an all-zero block), byte e + 127, and each code the
+ * E2M1 value nearest w * 2^-e (ties to the even code, saturating at 6, zero as
+ * code 0).  No tensor scale.  A non-finite weight latches QERL_ERR_NONFINITE.
+ */
+qerl_status qerl_mxfp4_quantize(const void *W, int64_t N, int64_t K, int64_t ldw, uint8_t *codes,
+                                uint8_t *scales, qerl_stream_t stream);
+
+/* y = x w_hat^T + s (x A^T) B^T with an MXFP4 weight, w_hat = e2m1(code) *
+ * 2^(scale byte - 127); x bf16 [M, K], A bf16 [r, K], B bf16 [N, r], y bf16
+ * [M, N], t_out (optional) FP32 [M, r].  ws (device): M * r * 4 bytes (rounded
+ * up to 256) unless t_out is given.  K % 32 == 0, 1 <= r <= 256. */
+qerl_status qerl_mxfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
+                                       const uint8_t *codes, const uint8_t *scales, const void *A,
+                                       const void *B, int r, float lora_scale, void *y, float *t_out,
+                                       void *ws, size_t ws_bytes, qerl_stream_t stream);
+
+/* qerl_nvfp4_lora_linear_fwd (standard code layout) with FP32 LoRA adapters:
+ * A (device) float [r, K], B (device) float [N, r]; t = x A^T and the LoRA
+ * term are accumulated in FP32.  ws as for qerl_mxfp4_lora_linear_fwd. */
+qerl_status qerl_nvfp4_lora_linear_fwd_f32ab(const void *x, int64_t M, int64_t K, int64_t N,
+                                             const uint8_t *codes, const uint8_t *scales,
+                                             const float *tensor_scale, const float *A, const float *B,
+                                             int r, float lora_scale, void *y, float *t_out, void *ws,
+                                             size_t ws_bytes, qerl_stream_t stream);
+
+/*
  * Decoder-layer chain at decode batch sizes: every NVFP4 + LoRA linear of n
  * Qwen2.5-style decoder layers, with the AQN-RMSNorms, the residual adds and
  * SwiGLU between them, in one persistent launch (one CTA per SM).  The chain
@@ -318,7 +358,7 @@ float qerl_aqn_sigma(int64_t step, int64_t total_steps, float sigma_start, float
  *     h2 = h1 + (silu(N2(h1) W_gate^T) * N2(h1) W_up^T) W_down^T (+ LoRA each),
  * N_i(h) = h * rsqrt(mean(h^2) + eps) * (gamma_i + sigma z_i), z ~ N(0,1) per
  * channel from Philox4x64-10 (key (seed, 2*layer + i - 1), counter
- * (channel / 4, step, 0, 0)), as qerl_aqn_rmsnorm (Box-Muller in FP32 here).
+ * (channel / 4, step, 0, 0)), as qerl_aqn_rmsnorm.
  * Attention itself is outside the path: `attn` is its output, given.  Each
  * linear's output is rounded to bf16, residual sums are rounded to bf16.
  * The norm is fused: its producer writes bf16(h * (gamma + sigma z)) and the

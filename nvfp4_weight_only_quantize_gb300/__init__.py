@@ -36,7 +36,8 @@ EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_lin
             "qerl_set_launch_chaining", "qerl_lora_linear_fwd_grouped_ws_bytes",
             "qerl_nvfp4_lora_linear_fwd_grouped",
             "qerl_launch_count", "qerl_decoder_chain_ws_bytes", "qerl_decoder_chain_plan",
-            "qerl_decoder_chain_run", "qerl_decoder_chain_destroy"]
+            "qerl_decoder_chain_run", "qerl_decoder_chain_destroy", "qerl_mxfp4_quantize",
+            "qerl_mxfp4_lora_linear_fwd", "qerl_nvfp4_lora_linear_fwd_f32ab"]
 
 
 class QerlError(RuntimeError):
@@ -92,6 +93,10 @@ def lib() -> C.CDLL:
             }
             sig["qerl_lora_linear_fwd_grouped_ws_bytes"] = ([i64, i64, i32, vp, i32], sz)
             sig["qerl_nvfp4_lora_linear_fwd_grouped"] = ([vp, i64, i64, i32, f32, vp, i32, i32, vp, sz, vp], i32)
+            sig["qerl_mxfp4_quantize"] = ([vp, i64, i64, i64, vp, vp, vp], i32)
+            sig["qerl_mxfp4_lora_linear_fwd"] = ([vp, i64, i64, i64, vp, vp, vp, vp, i32, f32, vp, vp, vp, sz, vp], i32)
+            sig["qerl_nvfp4_lora_linear_fwd_f32ab"] = ([vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, f32, vp, vp, vp,
+                                                        sz, vp], i32)
             sig["qerl_decoder_chain_ws_bytes"] = ([vp, i32], sz)
             sig["qerl_decoder_chain_plan"] = ([vp, i32, vp, vp, vp, vp, sz, vp], i32)
             sig["qerl_decoder_chain_run"] = ([vp, f32, u64, u64, u32, vp], i32)
@@ -291,6 +296,52 @@ def _bwd(name, dy, x, codes, scales, tensor_scale, A, B, lora_scale, t_saved, dx
                                 float(lora_scale), _p(t_saved), _p(dx), _p(dA), _p(dB), int(accumulate), _p(ws),
                                 ws.numel(), _stream(stream)), name)
     return dx, dA, dB
+
+
+# ---------------------------------------------------------------- format variants
+def qerl_mxfp4_quantize(W: torch.Tensor, out=None, stream=None):
+    """W bf16 [N, K] -> (codes u8 [N, K/2], E8M0 scales u8 [N, K/32])."""
+    assert W.dtype == torch.bfloat16 and W.dim() == 2 and W.stride(1) == 1
+    N, K = W.shape
+    if out is None:
+        out = (torch.empty(N, K // 2, dtype=torch.uint8, device=W.device),
+               torch.empty(N, K // 32, dtype=torch.uint8, device=W.device))
+    codes, scales = out
+    _check(lib().qerl_mxfp4_quantize(_p(W), N, K, W.stride(0), _p(codes), _p(scales), _stream(stream)),
+           "qerl_mxfp4_quantize")
+    return codes, scales
+
+
+def _t_ws(M, r, t_out, ws, device):
+    if t_out is None and ws is None:
+        ws = torch.empty(max(((M * r * 4 + 255) // 256) * 256, 1), dtype=torch.uint8, device=device)
+    return ws
+
+
+def qerl_mxfp4_lora_linear_fwd(x, codes, scales, A, B, lora_scale: float, y=None, t_out=None, ws=None, stream=None):
+    M, K = x.shape
+    N, r = B.shape
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
+    ws = _t_ws(M, r, t_out, ws, x.device)
+    _check(lib().qerl_mxfp4_lora_linear_fwd(_p(x), M, K, N, _p(codes), _p(scales), _p(A), _p(B), r, float(lora_scale),
+                                            _p(y), _p(t_out), _p(ws), 0 if ws is None else ws.numel(),
+                                            _stream(stream)), "qerl_mxfp4_lora_linear_fwd")
+    return y
+
+
+def qerl_nvfp4_lora_linear_fwd_f32ab(x, codes, scales, tensor_scale, A, B, lora_scale: float, y=None, t_out=None,
+                                     ws=None, stream=None):
+    """The forward with FP32 LoRA adapters A [r, K] and B [N, r] (float32)."""
+    assert A.dtype == torch.float32 and B.dtype == torch.float32
+    M, K = x.shape
+    N, r = B.shape
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
+    ws = _t_ws(M, r, t_out, ws, x.device)
+    _check(lib().qerl_nvfp4_lora_linear_fwd_f32ab(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A),
+                                                  _p(B), r, float(lora_scale), _p(y), _p(t_out), _p(ws),
+                                                  0 if ws is None else ws.numel(), _stream(stream)),
+           "qerl_nvfp4_lora_linear_fwd_f32ab")
+    return y
 
 
 # ---------------------------------------------------------------- AQN

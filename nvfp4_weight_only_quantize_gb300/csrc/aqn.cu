@@ -6,9 +6,10 @@
 // lives in the norm's scale parameters.  So the norm uses gamma + sigma * z with
 // one z[H] ~ N(0, 1) per (seed, step, layer), shared by every token.
 //
-// Two kernels: (1) the noise and the noisy scale vector, H/4 threads, each one
-// Philox4x64-10 block and two Box-Muller pairs in double precision; (2) the
-// bandwidth-bound RMSNorm, one CTA per token row.
+// One kernel for hidden sizes up to kFusedMaxH: every CTA draws the noisy scale
+// vector gamma + sigma z into shared memory (Philox4x64-10, Box-Muller in FP32)
+// and normalizes its token rows with it.  Wider rows take two kernels: the
+// noisy scale vector into the workspace, then the norm.
 #include "common.cuh"
 
 namespace qerl {
@@ -33,38 +34,56 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64
     }
 }
 
-// One thread per Box-Muller pair: thread 2i + p draws channels 4i + 2p and
-// 4i + 2p + 1 from Philox block i (both threads of a block compute it: the
-// FP64 transcendentals, not Philox, set the latency).  Writes any of z_out /
+// Box-Muller in FP32 from two Philox words: u1 = ((w0 >> 11) + 1) 2^-53 in
+// (0, 1], u2 = (w1 >> 11) 2^-53 in [0, 1); z = sqrt(-2 ln u1) (cos, sin)(2 pi u2).
+// ln u1 is taken as log1p(-(1 - u1)) near 1, where 1 - u1 (formed exactly in
+// integers) would round away in FP32.
+__device__ __forceinline__ void box_muller(uint64_t w0, uint64_t w1, float &z0, float &z1)
+{
+    const uint64_t a = (w0 >> 11) + 1ull;                 // u1 = a 2^-53, 1 <= a <= 2^53
+    const float lnu1 = a > (1ull << 52) ? log1pf(-(float)((1ull << 53) - a) * 0x1p-53f) : logf((float)a * 0x1p-53f);
+    const float rad = sqrtf(-2.0f * lnu1);
+    float sn, cs;
+    sincospif(2.0f * ((float)(w1 >> 11) * 0x1p-53f), &sn, &cs);
+    z0 = rad * cs;
+    z1 = rad * sn;
+}
+
+// The four normals of Philox block i (channels 4i .. 4i+3).
+__device__ __forceinline__ void noise4(uint64_t i, uint64_t seed, uint64_t step, uint32_t layer, float z[4],
+                                       uint64_t w[4])
+{
+    w[0] = i;
+    w[1] = step;
+    w[2] = 0ull;
+    w[3] = 0ull;
+    philox4x64_10(w, seed, (uint64_t)layer);
+    box_muller(w[0], w[1], z[0], z[1]);
+    box_muller(w[2], w[3], z[2], z[3]);
+}
+
+// One thread per Philox block: channels 4i .. 4i+3.  Writes any of z_out /
 // raw_out / scale_out given.
 __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32_t layer,
                                  const __nv_bfloat16 *__restrict__ gamma, float sigma, float *__restrict__ scale_out,
                                  float *__restrict__ z_out, uint64_t *__restrict__ raw_out)
 {
     pdl_trigger();
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t i = t >> 1;
-    const int p = (int)(t & 1);
-    if (4 * i + 2 * p >= H) return;
-    uint64_t w[4] = {(uint64_t)i, step, 0ull, 0ull};
-    philox4x64_10(w, seed, (uint64_t)layer);
-    const uint64_t w0 = p ? w[2] : w[0], w1 = p ? w[3] : w[1];
-    const double u1 = ((double)(w0 >> 11) + 1.0) * 0x1p-53;  // (0, 1]
-    const double u2 = (double)(w1 >> 11) * 0x1p-53;          // [0, 1)
-    const double rad = sqrt(-2.0 * log(u1));
-    double sn, cs;
-    sincospi(2.0 * u2, &sn, &cs);
-    const double z[2] = {rad * cs, rad * sn};
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (4 * i >= H) return;
+    float z[4];
+    uint64_t w[4];
+    noise4((uint64_t)i, seed, step, layer, z, w);
     // The draws need no input: only the writes (and gamma) wait for the
     // preceding work when the launch is chained.
     pdl_wait();
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int64_t c = 4 * i + 2 * p + e;
+    for (int e = 0; e < 4; ++e) {
+        const int64_t c = 4 * i + e;
         if (c >= H) break;
-        if (z_out) z_out[c] = (float)z[e];
-        if (raw_out) raw_out[c] = e ? w1 : w0;
-        if (scale_out) scale_out[c] = (float)((double)bf16f(gamma[c]) + (double)sigma * z[e]);
+        if (z_out) z_out[c] = z[e];
+        if (raw_out) raw_out[c] = w[e];
+        if (scale_out) scale_out[c] = bf16f(gamma[c]) + sigma * z[e];
     }
 }
 
@@ -145,6 +164,77 @@ __global__ void __launch_bounds__(kNormThreads)
     }
 }
 
+// AQN-RMSNorm in one launch: the CTA draws gamma + sigma z for all H channels
+// into shared memory (sigma = 0: gamma), then normalizes token rows m =
+// blockIdx.x, blockIdx.x + gridDim.x, ...
+constexpr int64_t kFusedMaxH = 16384;
+constexpr int kFusedThreads = 512;  // the noise of H = 3584 (896 Philox blocks) in at most two rounds
+__global__ void __launch_bounds__(kFusedThreads)
+    aqn_rmsnorm_fused_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t H,
+                             const __nv_bfloat16 *__restrict__ gamma, float eps, float sigma, uint64_t seed,
+                             uint64_t step, uint32_t layer, __nv_bfloat16 *__restrict__ y)
+{
+    extern __shared__ float gs[];  // [H]
+    __shared__ float red[32];
+    pdl_trigger();
+    pdl_wait();  // x, gamma and y follow the preceding work when the launch is chained
+    const int64_t nb = (H + 3) / 4;
+    const bool noisy = sigma != 0.0f;
+    for (int64_t i = threadIdx.x; i < nb; i += blockDim.x) {
+        float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        uint64_t w[4];
+        if (noisy) noise4((uint64_t)i, seed, step, layer, z, w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t c = 4 * i + e;
+            if (c < H) gs[c] = bf16f(gamma[c]) + sigma * z[e];
+        }
+    }
+    __syncthreads();
+    const bool vec = (H % 8) == 0;
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const __nv_bfloat16 *row = x + m * H;
+        __nv_bfloat16 *out = y + m * H;
+        float ss = 0.0f;
+        if (vec) {
+            for (int64_t v = threadIdx.x; v < H / 8; v += blockDim.x) {
+                const uint4 u = reinterpret_cast<const uint4 *>(row)[v];
+                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float a = bf16lo(wd[i]), b = bf16hi(wd[i]);
+                    ss = fmaf(a, a, ss);
+                    ss = fmaf(b, b, ss);
+                }
+            }
+        } else {
+            for (int64_t c = threadIdx.x; c < H; c += blockDim.x) {
+                const float a = bf16f(row[c]);
+                ss = fmaf(a, a, ss);
+            }
+        }
+        ss = block_sum(ss, red);
+        const float inv = rsqrtf(ss / (float)H + eps);
+        if (vec) {
+            for (int64_t v = threadIdx.x; v < H / 8; v += blockDim.x) {
+                const uint4 u = reinterpret_cast<const uint4 *>(row)[v];
+                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t c = v * 8 + 2 * i;
+                    const __nv_bfloat162 p = __floats2bfloat162_rn(bf16lo(wd[i]) * inv * gs[c], bf16hi(wd[i]) * inv * gs[c + 1]);
+                    o[i] = *reinterpret_cast<const uint32_t *>(&p);
+                }
+                reinterpret_cast<uint4 *>(out)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            for (int64_t c = threadIdx.x; c < H; c += blockDim.x) out[c] = __float2bfloat16_rn(bf16f(row[c]) * inv * gs[c]);
+        }
+        __syncthreads();  // red[] is reused by the next row
+    }
+}
+
 }  // namespace
 }  // namespace qerl
 
@@ -156,8 +246,8 @@ extern "C" qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, u
     if (H < 1 || !z_out) return QERL_ERR_INVALID_ARG;
     QERL_TRY(check_device());
     const int64_t n = (H + 3) / 4;
-    aqn_noise_kernel<<<(unsigned)((2 * n + 63) / 64), 64, 0, as_cuda(stream)>>>(H, seed, step, layer_id, nullptr,
-                                                                             0.0f, nullptr, z_out, raw_out);
+    aqn_noise_kernel<<<(unsigned)((n + 63) / 64), 64, 0, as_cuda(stream)>>>(H, seed, step, layer_id, nullptr, 0.0f,
+                                                                          nullptr, z_out, raw_out);
     return launched();
 }
 
@@ -173,11 +263,24 @@ extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, con
     if (noisy && (!ws || ws_bytes < qerl_workspace_bytes(QERL_OP_AQN_RMSNORM, M, 0, H, 0))) return QERL_ERR_WORKSPACE;
     QERL_TRY(check_device());
     cudaStream_t s = as_cuda(stream);
+    if (H <= kFusedMaxH) {  // one launch: every CTA draws the noisy scale into shared memory
+        int64_t g = M;
+        if (g > 2 * num_sms()) g = 2 * num_sms();
+        const size_t smem = (size_t)H * sizeof(float);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(aqn_rmsnorm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
+            return QERL_ERR_CUDA;
+        return launched(launch_k(aqn_rmsnorm_fused_kernel, dim3((unsigned)g), dim3(kFusedThreads), smem, s,
+                                 g_chain.load() != 0, static_cast<const __nv_bfloat16 *>(x), M, H,
+                                 static_cast<const __nv_bfloat16 *>(gamma), eps, sigma, seed, step, layer_id,
+                                 static_cast<__nv_bfloat16 *>(y)));
+    }
     float *gscale = nullptr;
     if (noisy) {
         gscale = static_cast<float *>(ws);
         const int64_t n = (H + 3) / 4;
-        QERL_TRY(launched(launch_k(aqn_noise_kernel, dim3((unsigned)((2 * n + 63) / 64)), dim3(64), 0, s,
+        QERL_TRY(launched(launch_k(aqn_noise_kernel, dim3((unsigned)((n + 63) / 64)), dim3(64), 0, s,
                                    g_chain.load() != 0, H, seed, step, layer_id,
                                    static_cast<const __nv_bfloat16 *>(gamma), sigma, gscale, (float *)nullptr,
                                    (uint64_t *)nullptr)));

@@ -120,13 +120,15 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64
         k1 += 0xBB67AE8584CAA73Bull;
     }
 }
+// u1 = ((w0 >> 11) + 1) 2^-53, u2 = (w1 >> 11) 2^-53; ln u1 as log1p(-(1 - u1))
+// near 1, where 1 - u1 (formed exactly in integers) would round away in FP32.
 __device__ __forceinline__ void box_muller_f32(uint64_t w0, uint64_t w1, float &z0, float &z1)
 {
-    const float u1 = (float)((double)((w0 >> 11) + 1ull) * 0x1p-53);  // (0, 1]
-    const float u2 = (float)((double)(w1 >> 11) * 0x1p-53);           // [0, 1)
-    const float rad = sqrtf(-2.0f * logf(u1));
+    const uint64_t a = (w0 >> 11) + 1ull;
+    const float lnu1 = a > (1ull << 52) ? log1pf(-(float)((1ull << 53) - a) * 0x1p-53f) : logf((float)a * 0x1p-53f);
+    const float rad = sqrtf(-2.0f * lnu1);
     float sn, cs;
-    sincospif(2.0f * u2, &sn, &cs);
+    sincospif(2.0f * ((float)(w1 >> 11) * 0x1p-53f), &sn, &cs);
     z0 = rad * cs;
     z1 = rad * sn;
 }

@@ -63,6 +63,26 @@ __device__ __forceinline__ float wprime(const uint8_t *codes, const uint8_t *sca
     }
     return e2m1_to_float(c) * e4m3_to_float(scales[n * (K / 16) + k / 16]);
 }
+// MXFP4 weight element: e2m1(code) * 2^(E8M0 byte - 127), blocks of 32 along k.
+__device__ __forceinline__ float wprime_mx(const uint8_t *codes, const uint8_t *scales, int64_t K, int64_t n,
+                                          int64_t k)
+{
+    const uint32_t byte = codes[n * (K / 2) + k / 2];
+    const uint32_t c = (k & 1) ? (byte >> 4) : (byte & 15u);
+    const uint32_t b = scales[n * (K / 32) + k / 32];
+    const float sc = b != 0u ? __uint_as_float(b << 23) : __uint_as_float(1u << 22);  // 2^(b-127); b = 0: 2^-127
+    return e2m1_to_float(c) * sc;
+}
+struct WRowMX {  // (n, k)
+    const uint8_t *codes, *scales;
+    int64_t K;
+    __device__ float operator()(int64_t n, int64_t k) const { return wprime_mx(codes, scales, K, n, k); }
+};
+struct RowF32 {  // (p, k) -> base[p * ld + k]
+    const float *base;
+    int64_t ld;
+    __device__ float operator()(int64_t p, int64_t k) const { return base[p * ld + k]; }
+};
 struct WRow {  // (n, k)
     const uint8_t *codes, *scales;
     int64_t K;
@@ -103,6 +123,23 @@ struct FwdEpi {
         float l = 0.0f;
         for (int j = 0; j < r; ++j) l = fmaf(t[m * r + j], bf16f(B[n * r + j]), l);
         y[m * N + n] = __float2bfloat16_rn(fmaf(s, l, *ts * acc));
+    }
+};
+// The forward's epilogue with FP32 LoRA B and/or no tensor scale (ts == null: 1).
+struct FwdEpiF32 {
+    __nv_bfloat16 *y;
+    int64_t N;
+    const float *ts;
+    const float *t;
+    const float *B32;            // FP32 [N, r], or null
+    const __nv_bfloat16 *B16;    // bf16 [N, r] when B32 is null
+    int r;
+    float s;
+    __device__ void operator()(int64_t m, int64_t n, float acc, int) const
+    {
+        float l = 0.0f;
+        for (int j = 0; j < r; ++j) l = fmaf(t[m * r + j], B32 ? B32[n * r + j] : bf16f(B16[n * r + j]), l);
+        y[m * N + n] = __float2bfloat16_rn(fmaf(s, l, (ts ? *ts : 1.0f) * acc));
     }
 };
 // dx[m, k] = s_t * acc + s * sum_j v[m, j] * A[j, k]
@@ -1086,4 +1123,58 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_grouped(const void *x, int64_t
         QERL_TRY(st);
     }
     return QERL_OK;
+}
+
+namespace {
+qerl_status variant_args(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes, const uint8_t *scales,
+                         const void *A, const void *B, int r, void *y, float *t_out, void *ws, size_t ws_bytes,
+                         int kmul)
+{
+    if (!codes || !scales || !A || !B) return QERL_ERR_INVALID_ARG;
+    if (M < 0 || K < 1 || N < 1) return QERL_ERR_INVALID_ARG;
+    if (K % kmul != 0 || r < 1 || r > 256) return QERL_ERR_SHAPE;
+    if (M == 0) return QERL_OK;
+    if (!x || !y) return QERL_ERR_INVALID_ARG;
+    if (!t_out && (!ws || ws_bytes < round256(size_t(M) * r * sizeof(float)))) return QERL_ERR_WORKSPACE;
+    return QERL_OK;
+}
+}  // namespace
+
+// MXFP4 weight (codes [N, K/2], E8M0 scales [N, K/32]), bf16 LoRA; CUDA cores.
+extern "C" qerl_status qerl_mxfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
+                                                  const uint8_t *codes, const uint8_t *scales, const void *A,
+                                                  const void *B, int r, float lora_scale, void *y, float *t_out,
+                                                  void *ws, size_t ws_bytes, qerl_stream_t stream)
+{
+    QERL_TRY(variant_args(x, M, K, N, codes, scales, A, B, r, y, t_out, ws, ws_bytes, 32));
+    if (M == 0) return QERL_OK;
+    QERL_TRY(check_device());
+    cudaStream_t s = as_cuda(stream);
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    float *t = t_out ? t_out : static_cast<float *>(ws);
+    QERL_TRY(run_gemm(M, (int64_t)r, K, RowBF16{xb, K}, RowBF16{static_cast<const __nv_bfloat16 *>(A), K},
+                      StoreF32{t, r, 1.0f, 0}, s));
+    return run_gemm(M, N, K, RowBF16{xb, K}, WRowMX{codes, scales, K},
+                    FwdEpiF32{static_cast<__nv_bfloat16 *>(y), N, nullptr, t, nullptr,
+                              static_cast<const __nv_bfloat16 *>(B), r, lora_scale},
+                    s);
+}
+
+// NVFP4 weight with FP32 LoRA adapters A [r, K], B [N, r]; CUDA cores.
+extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_f32ab(const void *x, int64_t M, int64_t K, int64_t N,
+                                                        const uint8_t *codes, const uint8_t *scales,
+                                                        const float *tensor_scale, const float *A, const float *B,
+                                                        int r, float lora_scale, void *y, float *t_out, void *ws,
+                                                        size_t ws_bytes, qerl_stream_t stream)
+{
+    if (!tensor_scale) return QERL_ERR_INVALID_ARG;
+    QERL_TRY(variant_args(x, M, K, N, codes, scales, A, B, r, y, t_out, ws, ws_bytes, 16));
+    if (M == 0) return QERL_OK;
+    QERL_TRY(check_device());
+    cudaStream_t s = as_cuda(stream);
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    float *t = t_out ? t_out : static_cast<float *>(ws);
+    QERL_TRY(run_gemm(M, (int64_t)r, K, RowBF16{xb, K}, RowF32{A, K}, StoreF32{t, r, 1.0f, 0}, s));
+    return run_gemm(M, N, K, RowBF16{xb, K}, WRow{codes, scales, K, 0},
+                    FwdEpiF32{static_cast<__nv_bfloat16 *>(y), N, tensor_scale, t, B, nullptr, r, lora_scale}, s);
 }

@@ -175,6 +175,51 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
 }
 
+// MXFP4 (bitsofall "NVFP4" section: MXFP4's blocks are 32 values with a
+// power-of-two scale; OCP MX rule for that scale): one 32-block per thread,
+// e = floor(log2(amax)) - 2 clamped to [-127, 127] (all-zero block: -127),
+// scale byte e + 127, codes = E2M1 nearest of w * 2^-e.  One pass over W.
+__global__ void __launch_bounds__(kQuantThreads)
+    mx_quantize_kernel(const __nv_bfloat16 *__restrict__ W, int64_t N, int64_t K, int64_t ldw,
+                       uint8_t *__restrict__ codes, uint8_t *__restrict__ scales, unsigned int *err)
+{
+    const int64_t bpr = K / 32;
+    const int64_t nblk = N * bpr;
+    for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblk;
+         blk += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t row = blk / bpr, b = blk - row * bpr;
+        const __nv_bfloat16 *src = W + row * ldw + b * 32;
+        uint4 u[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) u[v] = ld_stream(src + 8 * v);
+        uint32_t m = 0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) m = max(max(m, mag2(u[v].x)), max(mag2(u[v].y), max(mag2(u[v].z), mag2(u[v].w))));
+        if (m >= 0x7F80u) {  // Inf or NaN in the block
+            latch_error(err, QERL_ERR_NONFINITE);
+            continue;
+        }
+        int e = -127;
+        if (m != 0u) {
+            int ex;
+            frexpf(__uint_as_float(m << 16), &ex);  // amax = f 2^ex, f in [0.5, 1)
+            e = min(127, max(-127, ex - 3));
+        }
+        uint32_t wc[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint32_t wd[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
+            uint32_t c = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                c |= (e2m1_code(ldexpf(bf16lo(wd[i]), -e)) | (e2m1_code(ldexpf(bf16hi(wd[i]), -e)) << 4)) << (8 * i);
+            wc[v] = c;
+        }
+        *reinterpret_cast<uint4 *>(codes + row * (K / 2) + b * 16) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
+        scales[row * bpr + b] = (uint8_t)(e + 127);
+    }
+}
+
 __global__ void dequantize_kernel(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales,
                                   const float *__restrict__ tensor_scale, int64_t N, int64_t K,
                                   __nv_bfloat16 *__restrict__ out, int apply_ts)
@@ -272,5 +317,21 @@ extern "C" qerl_status qerl_nvfp4_dequantize(const uint8_t *codes, const uint8_t
     dequantize_kernel<<<(unsigned)g, 256, 0, as_cuda(stream)>>>(codes, scales, tensor_scale, N, K,
                                                                  static_cast<__nv_bfloat16 *>(W_out),
                                                                  apply_tensor_scale);
+    return launched();
+}
+
+extern "C" qerl_status qerl_mxfp4_quantize(const void *W, int64_t N, int64_t K, int64_t ldw, uint8_t *codes,
+                                           uint8_t *scales, qerl_stream_t stream)
+{
+    if (!W || !codes || !scales) return QERL_ERR_INVALID_ARG;
+    if (N < 1 || K < 1 || ldw < K) return N < 0 || K < 0 ? QERL_ERR_INVALID_ARG : QERL_ERR_SHAPE;
+    if (K % 32 != 0) return QERL_ERR_SHAPE;
+    if (!aligned16(W) || (ldw * 2) % 16 != 0 || !aligned16(codes)) return QERL_ERR_ALIGN;
+    QERL_TRY(check_device());
+    const int64_t nblk = N * (K / 32);
+    int64_t g = (nblk + kQuantThreads - 1) / kQuantThreads;
+    if (g > 16 * num_sms()) g = 16 * num_sms();
+    mx_quantize_kernel<<<(unsigned)g, kQuantThreads, 0, as_cuda(stream)>>>(static_cast<const __nv_bfloat16 *>(W), N, K,
+                                                                          ldw, codes, scales, error_word());
     return launched();
 }

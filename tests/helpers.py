@@ -6,7 +6,9 @@ tolerance checks.  Tolerances:
   - AQN-RMSNorm: |got - ref| <= 2e-3 * (|ref| + rms(ref)) + ulp_bf16(ref) / 2; the
     half ulp is the rounding of the bf16 result itself (up to 2^-8 relative), which
     no bf16 output can avoid and which is larger than 2e-3 in the low part of a
-    binade; noise z: 1e-6 absolute.
+    binade; noise z: 1e-5 absolute (FP32 Box-Muller against the fp64 oracle:
+    the log, the sine/cosine and the FP32 forms of u1 and u2 each err by about
+    one part in 2^24 of values up to 8.6, a few 1e-6 at most).
 """
 import numpy as np
 import torch
@@ -17,6 +19,7 @@ from nvfp4_weight_only_quantize_gb300 import synth
 LIN_TOL = 1e-2
 _QUANT_CACHE = {}  # the oracle's quantization of the 8 most recent weights
 NORM_TOL = 2e-3
+Z_TOL = 1e-5
 
 
 def half_ulp_bf16(ref):

@@ -6,7 +6,7 @@ import torch
 import oracle
 import nvfp4_weight_only_quantize_gb300 as q
 from nvfp4_weight_only_quantize_gb300 import synth
-from helpers import NORM_TOL, assert_rel_rms, f64
+from helpers import NORM_TOL, Z_TOL, assert_rel_rms, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -16,7 +16,7 @@ def test_noise_words_bit_exact_and_values(H, seed, step, layer):
     z, raw = q.qerl_aqn_noise(H, seed, step, layer, want_raw=True)
     oz, oraw = oracle.aqn_noise(H, seed, step, layer, want_raw=True)
     np.testing.assert_array_equal(raw.cpu().numpy().view(np.uint64), oraw)
-    np.testing.assert_allclose(z.double().cpu().numpy(), oz, rtol=0, atol=1e-6)
+    np.testing.assert_allclose(z.double().cpu().numpy(), oz, rtol=0, atol=Z_TOL)
 
 
 @pytest.mark.parametrize("M,H,sigma", [(1, 3584, 1e-2), (8, 3584, 5e-4), (64, 3584, 0.0), (3, 100, 0.05),
