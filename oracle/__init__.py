@@ -97,6 +97,9 @@ def lib():
             L.orc_aqn_rmsnorm.argtypes = [_u16, i64, i64, _u16, f64, f64, u64, u64, u32,
                                           _i64, i64, _f64]
             L.orc_aqn_rmsnorm.restype = None
+            L.orc_aqn_rmsnorm_mode.argtypes = [_u16, i64, i64, _u16, f64, f64, u64, u64, u32, C.c_int,
+                                               _i64, i64, _f64]
+            L.orc_aqn_rmsnorm_mode.restype = None
             L.orc_aqn_sigma.argtypes = [i64, i64, f64, f64, i32]
             L.orc_aqn_sigma.restype = f64
             _lib = L
@@ -264,13 +267,19 @@ def aqn_noise(H, seed, step, layer, want_raw=False):
     return (z, raw) if want_raw else z
 
 
-def aqn_rmsnorm(x_bits, gamma_bits, eps, sigma, seed, step, layer, rows=None):
+def aqn_rmsnorm(x_bits, gamma_bits, eps, sigma, seed, step, layer, rows=None, multiplicative=False):
+    """Noise added to the scale (gamma + sigma z), or with multiplicative=True
+    scaling it (gamma (1 + sigma z))."""
     x_bits = _c(x_bits, np.uint16)
     M, H = x_bits.shape
     rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
     y = np.zeros((len(rows), H), np.float64)
-    lib().orc_aqn_rmsnorm(x_bits, M, H, _c(gamma_bits, np.uint16), float(eps), float(sigma),
-                          seed, step, layer, rows, len(rows), y)
+    if multiplicative:
+        lib().orc_aqn_rmsnorm_mode(x_bits, M, H, _c(gamma_bits, np.uint16), float(eps), float(sigma),
+                                   seed, step, layer, 1, rows, len(rows), y)
+    else:
+        lib().orc_aqn_rmsnorm(x_bits, M, H, _c(gamma_bits, np.uint16), float(eps), float(sigma),
+                              seed, step, layer, rows, len(rows), y)
     return y
 
 

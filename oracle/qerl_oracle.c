@@ -557,10 +557,14 @@ void orc_aqn_noise(int64_t H, uint64_t seed, uint64_t step, uint32_t layer,
 /* AQN-RMSNorm: y[m, c] = x[m, c] / sqrt(mean_c x^2 + eps) * (gamma[c] + sigma * z[c])
  * [AQN-S][AQN-M], fp64, for the nrows token rows listed in rows[]; y is
  * [nrows, H]. */
-void orc_aqn_rmsnorm(const uint16_t *x, int64_t M, int64_t H,
-                     const uint16_t *gamma, double eps, double sigma,
-                     uint64_t seed, uint64_t step, uint32_t layer,
-                     const int64_t *rows, int64_t nrows, double *y)
+/* AQN-RMSNorm with the noise on the scale parameter, in one of the two
+ * readings of "Gaussian noise in the LayerNorm scale" (dataforcee, AQN
+ * paragraph): mult = 0 adds it, scale gamma + sigma z; mult = 1 scales by it,
+ * gamma (1 + sigma z). */
+void orc_aqn_rmsnorm_mode(const uint16_t *x, int64_t M, int64_t H,
+                          const uint16_t *gamma, double eps, double sigma,
+                          uint64_t seed, uint64_t step, uint32_t layer, int mult,
+                          const int64_t *rows, int64_t nrows, double *y)
 {
     int64_t i, c;
     double *z = (double *)malloc((size_t)(H > 0 ? H : 1) * sizeof(double));
@@ -572,11 +576,22 @@ void orc_aqn_rmsnorm(const uint16_t *x, int64_t M, int64_t H,
         for (c = 0; c < H; ++c)
             ss += orc_bf16_value(row[c]) * orc_bf16_value(row[c]);
         inv = 1.0 / sqrt(ss / (double)H + eps);
-        for (c = 0; c < H; ++c)
-            y[i * H + c] = orc_bf16_value(row[c]) * inv *
-                           (orc_bf16_value(gamma[c]) + sigma * z[c]);
+        for (c = 0; c < H; ++c) {
+            const double g = orc_bf16_value(gamma[c]);
+            const double scale = mult ? g * (1.0 + sigma * z[c]) : g + sigma * z[c];
+            y[i * H + c] = orc_bf16_value(row[c]) * inv * scale;
+        }
     }
     free(z);
+}
+
+/* The additive reading (the library's default). */
+void orc_aqn_rmsnorm(const uint16_t *x, int64_t M, int64_t H,
+                     const uint16_t *gamma, double eps, double sigma,
+                     uint64_t seed, uint64_t step, uint32_t layer,
+                     const int64_t *rows, int64_t nrows, double *y)
+{
+    orc_aqn_rmsnorm_mode(x, M, H, gamma, eps, sigma, seed, step, layer, 0, rows, nrows, y);
 }
 
 /* Exponential-decay noise schedule [AQN-S][Hints]: num_stages equal stages over

@@ -90,6 +90,25 @@ def test_rmsnorm_noise_enters_the_scale_additively():
     np.testing.assert_allclose(y, ref, rtol=1e-12)
 
 
+def test_rmsnorm_noise_scales_the_scale_multiplicatively():
+    """The other reading of noise in the norm's scale: y = rms_norm(x) with
+    weight gamma * (1 + sigma z), against torch's rms_norm; with gamma = 1 the
+    two readings coincide, and with sigma = 0 both are plain RMSNorm."""
+    x = synth.activations(3, 24, 5)
+    g = synth.norm_gamma(24, 6)
+    sigma = 0.01
+    y = oracle.aqn_rmsnorm(synth.bits(x), synth.bits(g), 1e-6, sigma, 11, 12, 13, multiplicative=True)
+    z = torch.from_numpy(oracle.aqn_noise(24, 11, 12, 13))
+    ref = torch.nn.functional.rms_norm(x.double(), (24,), weight=g.double() * (1 + sigma * z), eps=1e-6).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12)
+    ones = np.full(24, 0x3F80, np.uint16)
+    np.testing.assert_array_equal(oracle.aqn_rmsnorm(synth.bits(x), ones, 1e-6, sigma, 1, 2, 3, multiplicative=True),
+                                  oracle.aqn_rmsnorm(synth.bits(x), ones, 1e-6, sigma, 1, 2, 3))
+    np.testing.assert_array_equal(oracle.aqn_rmsnorm(synth.bits(x), synth.bits(g), 1e-6, 0.0, 1, 2, 3,
+                                                     multiplicative=True),
+                                  oracle.aqn_rmsnorm(synth.bits(x), synth.bits(g), 1e-6, 0.0, 1, 2, 3))
+
+
 def test_sigma_schedule():
     s0, s1, S, T = 1e-2, 5e-4, 10, 1000
     vals = [oracle.aqn_sigma(t, T, s0, s1, S) for t in range(T)]
