@@ -520,7 +520,8 @@ def decode_rows(dev):
                    "tokens_per_s": round(M / us * 1e6, 1)}
         del graphs, buf
     out["c1_decode_by_M"] = {"workload": wl.name + " (per-linear kernels, one graph per step)", "by_M": by_m}
-    # crossover: gate_proj at M = 1..8, CUDA-core GEMV against the tcgen05 path
+    # crossover: gate_proj at M = 1..8: the CUDA-core GEMM, the CUDA-core GEMV
+    # (M <= 2) and the tcgen05 path
     cross = {}
     name, N, K = [l for l in wl.linears if l[0] == "gate_proj"][0]
     li = [l[0] for l in wl.linears].index(name)
@@ -529,7 +530,8 @@ def decode_rows(dev):
         yout = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         wsl = q.workspace(q.OP_LINEAR_FWD, M, N, K, wl.r, dev)
         row = {}
-        for tag, algo in (("simt", q.ALGO_SIMT), ("tcgen05", q.ALGO_TCGEN05)):
+        algos = [("simt", q.ALGO_SIMT), ("tcgen05", q.ALGO_TCGEN05)] + ([("gemv", q.ALGO_GEMV)] if M <= 2 else [])
+        for tag, algo in algos:
             q.set_linear_algo(algo)
 
             def run_lin(xin=xin, yout=yout, wsl=wsl):
@@ -541,11 +543,12 @@ def decode_rows(dev):
             row[tag + "_us"] = round(_time_graph(g, 10) / (10 * n_copies) * 1e6, 2)
             del g
         q.set_linear_algo(q.ALGO_AUTO)
-        row["faster"] = min(("simt", "tcgen05"), key=lambda t: row[t + "_us"])
+        row["fastest"] = min([t for t, _ in algos], key=lambda t: row[t + "_us"])
+        row["GBps_fastest"] = round(linear_bytes(N, K, wl.r) / (row[row["fastest"] + "_us"] * 1e3), 1)
         cross[M] = row
     out["c1_crossover_gate_proj"] = {"workload": f"qwen2.5-7b gate_proj {N}x{K}, {n_copies} rotating copies",
                                      "by_M": cross,
-                                     "auto": "the library takes the tensor-core path for every M at these shapes"}
+                                     "auto": "AUTO takes the GEMV at M <= 2 and the tensor-core path above"}
     del layer
     torch.cuda.empty_cache()
     # the decoder-chain kernel on one 7B layer (norms, residuals and SwiGLU fused), 4 rotating layers
@@ -618,9 +621,60 @@ def other_rows(dev, only=None, profile=False):
     sec = timed(lambda: q.qerl_nvfp4_quantize(W, out=(codes, scales, ts), ws=wsq), 20) if want("a1") else 0.0
     if want("a1"):
         rows["a1_quantize"] = {"workload": f"qwen2.5-7b gate_proj weight {N}x{K} bf16", "us": round(sec * 1e6, 1),
-                           "GBps": round(N * K * 2.5625 / sec / 1e9, 1),
-                               "bytes": "2 B read + 0.5625 B written per weight (the kernel reads W twice)"}
+                               "GBps": round(N * K * 2.5625 / sec / 1e9, 1),
+                               "bytes": "2 B read + 0.5625 B written per weight (W is read twice; the second, "
+                                        "backward pass finds its first part in L2)"}
+        # f3: MXFP4 quantization of the same weight (one pass: blocks of 32, power-of-two scales)
+        mcodes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+        mscales = torch.empty(N, K // 32, dtype=torch.uint8, device=dev)
+        sec = timed(lambda: q.qerl_mxfp4_quantize(W, out=(mcodes, mscales)), 20)
+        rows["f3_mxfp4_quantize"] = {"workload": f"qwen2.5-7b gate_proj weight {N}x{K} bf16",
+                                     "us": round(sec * 1e6, 1),
+                                     "GBps": round(N * K * (2 + 0.5 + 1 / 32) / sec / 1e9, 1),
+                                     "bytes": "2 B read + 0.53125 B written per weight"}
+        del mcodes, mscales
+        # an L2-sized weight (q_proj 3584 x 3584, 25.7 MB), 8 rotating copies so each call starts cold
+        N2, K2, nc = 3584, 3584, 8
+        Ws = [synth.weight(N2, K2, 30 + c, dev) for c in range(nc)]
+        outs = [(torch.empty(N2, K2 // 2, dtype=torch.uint8, device=dev),
+                 torch.empty(N2, K2 // 16, dtype=torch.uint8, device=dev),
+                 torch.empty(1, dtype=torch.float32, device=dev)) for _ in range(nc)]
+        wsq2 = q.workspace(q.OP_QUANTIZE, 0, N2, K2, 0, dev)
+        sec = timed(lambda: [q.qerl_nvfp4_quantize(Ws[c], out=outs[c], ws=wsq2) for c in range(nc)], 10) / nc
+        rows["a1_quantize_l2_sized"] = {"workload": f"qwen2.5-7b q_proj weight {N2}x{K2} bf16, {nc} rotating copies",
+                                        "us": round(sec * 1e6, 1), "GBps": round(N2 * K2 * 2.5625 / sec / 1e9, 1),
+                                        "bytes": "2 B read + 0.5625 B written per weight"}
+        del Ws, outs
     del W
+    # f3: the forwards with an MXFP4 weight and with FP32 LoRA adapters (CUDA-core
+    # GEMM), beside the NVFP4 forward, on qwen2.5-7b gate_proj at M = 8, r = 32
+    if want("f3"):
+        N, K, M, r = 18944, 3584, 8, 32
+        W = synth.weight(N, K, 11, dev)
+        ncodes, nscales, nts = q.qerl_nvfp4_quantize(W)
+        mcodes, mscales = q.qerl_mxfp4_quantize(W)
+        del W
+        x = synth.activations(M, K, 14, dev)
+        A, B = synth.lora_A(r, K, 15, dev), synth.lora_B(N, r, 16, dev)
+        Af, Bf = A.float(), B.float()
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        wsl = q.workspace(q.OP_LINEAR_FWD, M, N, K, r, dev)
+        arms = {"nvfp4_bf16_adapters": lambda: q.qerl_nvfp4_lora_linear_fwd(x, ncodes, nscales, nts, A, B, 2.0, y=y,
+                                                                            ws=wsl),
+                "nvfp4_fp32_adapters": lambda: q.qerl_nvfp4_lora_linear_fwd_f32ab(x, ncodes, nscales, nts, Af, Bf, 2.0,
+                                                                              y=y, ws=wsl),
+                "mxfp4_bf16_adapters": lambda: q.qerl_mxfp4_lora_linear_fwd(x, mcodes, mscales, A, B, 2.0, y=y,
+                                                                            ws=wsl)}
+        res = {}
+        for name, fn in arms.items():
+            sec = timed(fn, 10)
+            wbytes = N * K * (0.5 + (1 / 32 if name.startswith("mx") else 1 / 16))
+            res[name] = {"us": round(sec * 1e6, 1), "weight_GBps": round(wbytes / sec / 1e9, 1)}
+        rows["f3_format_variants_fwd"] = {"workload": f"qwen2.5-7b gate_proj {N}x{K}, M={M}, r={r}",
+                                          "by_format": res,
+                                          "path": "NVFP4 with bf16 adapters on tcgen05; the FP32-adapter and MXFP4 "
+                                                  "forwards on the CUDA-core GEMM"}
+        del ncodes, nscales, nts, mcodes, mscales
     # a2: decode and prefill norms
     for M, H, tag in ([(64, 3584, "decode M=64 H=3584"), (4096, 5120, "prefill M=4096 H=5120")] if want("a2") else []):
         x = synth.activations(M, H, 12, dev)
@@ -831,7 +885,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize/norm/prefill/backward lines")
-    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5", "f2"],
+    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5", "f2", "f3"],
                     help="run only that row's measurement, its timed launches bracketed by "
                          "cudaProfilerStart/Stop (for ncu --profile-from-start off), and print it")
     ap.add_argument("--codes", default="packed", choices=["packed", "standard"],

@@ -76,8 +76,13 @@ enum {
     QERL_OP_AQN_RMSNORM = 3
 };
 
-/* Linear algorithm selection (qerl_set_linear_algo); AUTO is the default. */
-enum { QERL_ALGO_AUTO = 0, QERL_ALGO_SIMT = 1, QERL_ALGO_TCGEN05 = 2 };
+/* Linear algorithm selection (qerl_set_linear_algo); AUTO is the default.
+ * AUTO: a single-token forward on a weight of at most 24M values runs the
+ * CUDA-core GEMV (where it applies: K % 32 == 0, r <= 256, M * (K + r) * 4
+ * bytes <= 200 KiB; not in grouped calls); other calls run the tensor-core
+ * kernels where they apply, else the CUDA-core GEMM.  GEMV selects the GEMV
+ * for every forward of one or two tokens it applies to. */
+enum { QERL_ALGO_AUTO = 0, QERL_ALGO_SIMT = 1, QERL_ALGO_TCGEN05 = 2, QERL_ALGO_GEMV = 3 };
 
 /*
  * NVFP4 quantization of a bf16 weight (bitsofall, "NVFP4: NVIDIA's FP4 Format":
@@ -288,6 +293,20 @@ qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *ga
                              void *y, void *ws, size_t ws_bytes, qerl_stream_t stream);
 
 /*
+ * The same norm with the noise mode chosen (dataforcee, AQN paragraph: noise in
+ * the norm's scale parameters, which reads two ways):
+ *   QERL_AQN_NOISE_ADD  scale gamma[c] + sigma * z[c]   (qerl_aqn_rmsnorm)
+ *   QERL_AQN_NOISE_MUL  scale gamma[c] * (1 + sigma * z[c])
+ * Any other noise_mode returns QERL_ERR_INVALID_ARG.  Arguments, workspace and
+ * launches as qerl_aqn_rmsnorm.
+ */
+enum { QERL_AQN_NOISE_ADD = 0, QERL_AQN_NOISE_MUL = 1 };
+qerl_status qerl_aqn_rmsnorm_mode(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
+                                  float sigma, uint64_t seed, uint64_t step, uint32_t layer_id,
+                                  int noise_mode, void *y, void *ws, size_t ws_bytes,
+                                  qerl_stream_t stream);
+
+/*
  * The AQN noise vector alone (test aid): z_out (device) float [H]; raw_out
  * (device, optional) uint64 [H], the Philox word each channel used:
  * block i = c/4 -> words w0..w3 of Philox4x64-10(counter (i, step, 0, 0),
@@ -430,8 +449,10 @@ qerl_status qerl_get_error(qerl_stream_t stream);
 /* Static description of a status code. */
 const char *qerl_status_string(qerl_status status);
 
-/* Selects the linear kernels (process-wide): QERL_ALGO_AUTO, _SIMT or _TCGEN05.
- * TCGEN05 falls back to SIMT for shapes it does not cover. */
+/* Selects the linear kernels (process-wide): QERL_ALGO_AUTO, _SIMT, _TCGEN05 or
+ * _GEMV.  TCGEN05 falls back to SIMT for shapes it does not cover; GEMV (the
+ * forward only; the backward runs as under AUTO) falls back to the AUTO choice
+ * among the other two. */
 qerl_status qerl_set_linear_algo(int algo);
 
 /* Number of kernels this library launched since load (host-side counter). */

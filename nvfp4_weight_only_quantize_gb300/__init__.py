@@ -25,13 +25,15 @@ STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARG", 2: "QERL_ERR_SHAPE", 3:
 NOALLOC_SCRATCH_BYTES = 8 << 20  # QERL_NOALLOC_SCRATCH_BYTES
 SCALE_ROUND_UP, SCALE_ROUND_NEAREST_EVEN = 0, 1
 OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_AQN_RMSNORM = 0, 1, 2, 3
-ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05 = 0, 1, 2
+ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05, ALGO_GEMV = 0, 1, 2, 3
+AQN_NOISE_ADD, AQN_NOISE_MUL = 0, 1
 
 # Every C symbol include/qerl.h declares (checked by the CPU test suite).
 EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_linear_fwd",
             "qerl_nvfp4_lora_linear_fwd_noalloc", "qerl_nvfp4_pack_codes", "qerl_nvfp4_unpack_codes",
             "qerl_nvfp4_lora_linear_fwd_packed", "qerl_nvfp4_lora_linear_bwd_packed",
-            "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_noise", "qerl_aqn_sigma",
+            "qerl_nvfp4_lora_linear_bwd", "qerl_aqn_rmsnorm", "qerl_aqn_rmsnorm_mode", "qerl_aqn_noise",
+            "qerl_aqn_sigma",
             "qerl_workspace_bytes", "qerl_get_error", "qerl_status_string", "qerl_set_linear_algo",
             "qerl_set_launch_chaining", "qerl_lora_linear_fwd_grouped_ws_bytes",
             "qerl_nvfp4_lora_linear_fwd_grouped",
@@ -82,6 +84,7 @@ def lib() -> C.CDLL:
                 "qerl_nvfp4_pack_codes": ([vp, i64, i64, vp, vp], i32),
                 "qerl_nvfp4_unpack_codes": ([vp, i64, i64, vp, vp], i32),
                 "qerl_aqn_rmsnorm": ([vp, i64, i64, vp, f32, f32, u64, u64, u32, vp, vp, sz, vp], i32),
+                "qerl_aqn_rmsnorm_mode": ([vp, i64, i64, vp, f32, f32, u64, u64, u32, i32, vp, vp, sz, vp], i32),
                 "qerl_aqn_noise": ([i64, u64, u64, u32, vp, vp, vp], i32),
                 "qerl_aqn_sigma": ([i64, i64, f32, f32, i32], f32),
                 "qerl_workspace_bytes": ([i32, i64, i64, i64, i32], sz),
@@ -346,12 +349,19 @@ def qerl_nvfp4_lora_linear_fwd_f32ab(x, codes, scales, tensor_scale, A, B, lora_
 
 # ---------------------------------------------------------------- AQN
 def qerl_aqn_rmsnorm(x, gamma, eps: float, sigma: float, seed: int, step: int, layer_id: int, y=None, ws=None,
-                     stream=None):
+                     stream=None, noise_mode: int = None):
+    """noise_mode None: qerl_aqn_rmsnorm (additive); AQN_NOISE_ADD / AQN_NOISE_MUL:
+    qerl_aqn_rmsnorm_mode."""
     M, H = x.shape
     y = torch.empty_like(x) if y is None else y
     ws = workspace(OP_AQN_RMSNORM, M, 0, H, 0, x.device) if ws is None else ws
-    _check(lib().qerl_aqn_rmsnorm(_p(x), M, H, _p(gamma), float(eps), float(sigma), seed, step, layer_id, _p(y),
-                                  _p(ws), ws.numel(), _stream(stream)), "qerl_aqn_rmsnorm")
+    if noise_mode is None:
+        _check(lib().qerl_aqn_rmsnorm(_p(x), M, H, _p(gamma), float(eps), float(sigma), seed, step, layer_id, _p(y),
+                                      _p(ws), ws.numel(), _stream(stream)), "qerl_aqn_rmsnorm")
+    else:
+        _check(lib().qerl_aqn_rmsnorm_mode(_p(x), M, H, _p(gamma), float(eps), float(sigma), seed, step, layer_id,
+                                           int(noise_mode), _p(y), _p(ws), ws.numel(), _stream(stream)),
+               "qerl_aqn_rmsnorm_mode")
     return y
 
 

@@ -64,9 +64,16 @@ __device__ __forceinline__ void noise4(uint64_t i, uint64_t seed, uint64_t step,
 
 // One thread per Philox block: channels 4i .. 4i+3.  Writes any of z_out /
 // raw_out / scale_out given.
+// Noisy scale of channel c: gamma + sigma z (additive) or gamma (1 + sigma z).
+__device__ __forceinline__ float noisy_scale(float g, float sigma, float z, int mult)
+{
+    return mult ? g * (1.0f + sigma * z) : g + sigma * z;
+}
+
 __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32_t layer,
-                                 const __nv_bfloat16 *__restrict__ gamma, float sigma, float *__restrict__ scale_out,
-                                 float *__restrict__ z_out, uint64_t *__restrict__ raw_out)
+                                 const __nv_bfloat16 *__restrict__ gamma, float sigma, int mult,
+                                 float *__restrict__ scale_out, float *__restrict__ z_out,
+                                 uint64_t *__restrict__ raw_out)
 {
     pdl_trigger();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -83,7 +90,7 @@ __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32
         if (c >= H) break;
         if (z_out) z_out[c] = z[e];
         if (raw_out) raw_out[c] = w[e];
-        if (scale_out) scale_out[c] = bf16f(gamma[c]) + sigma * z[e];
+        if (scale_out) scale_out[c] = noisy_scale(bf16f(gamma[c]), sigma, z[e], mult);
     }
 }
 
@@ -164,15 +171,16 @@ __global__ void __launch_bounds__(kNormThreads)
     }
 }
 
-// AQN-RMSNorm in one launch: the CTA draws gamma + sigma z for all H channels
-// into shared memory (sigma = 0: gamma), then normalizes token rows m =
+// AQN-RMSNorm in one launch: the CTA draws the noisy scale (gamma + sigma z,
+// or gamma (1 + sigma z)) for all H channels into shared memory (sigma = 0:
+// gamma), then normalizes token rows m =
 // blockIdx.x, blockIdx.x + gridDim.x, ...
 constexpr int64_t kFusedMaxH = 16384;
 constexpr int kFusedThreads = 512;  // the noise of H = 3584 (896 Philox blocks) in at most two rounds
 __global__ void __launch_bounds__(kFusedThreads)
     aqn_rmsnorm_fused_kernel(const __nv_bfloat16 *__restrict__ x, int64_t M, int64_t H,
                              const __nv_bfloat16 *__restrict__ gamma, float eps, float sigma, uint64_t seed,
-                             uint64_t step, uint32_t layer, __nv_bfloat16 *__restrict__ y)
+                             uint64_t step, uint32_t layer, int mult, __nv_bfloat16 *__restrict__ y)
 {
     extern __shared__ float gs[];  // [H]
     __shared__ float red[32];
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(kFusedThreads)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int64_t c = 4 * i + e;
-            if (c < H) gs[c] = bf16f(gamma[c]) + sigma * z[e];
+            if (c < H) gs[c] = noisy_scale(bf16f(gamma[c]), sigma, z[e], mult);
         }
     }
     __syncthreads();
@@ -247,14 +255,17 @@ extern "C" qerl_status qerl_aqn_noise(int64_t H, uint64_t seed, uint64_t step, u
     QERL_TRY(check_device());
     const int64_t n = (H + 3) / 4;
     aqn_noise_kernel<<<(unsigned)((n + 63) / 64), 64, 0, as_cuda(stream)>>>(H, seed, step, layer_id, nullptr, 0.0f,
-                                                                          nullptr, z_out, raw_out);
+                                                                          0, nullptr, z_out, raw_out);
     return launched();
 }
 
-extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
-                                        float sigma, uint64_t seed, uint64_t step, uint32_t layer_id, void *y,
-                                        void *ws, size_t ws_bytes, qerl_stream_t stream)
+extern "C" qerl_status qerl_aqn_rmsnorm_mode(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
+                                             float sigma, uint64_t seed, uint64_t step, uint32_t layer_id,
+                                             int noise_mode, void *y, void *ws, size_t ws_bytes,
+                                             qerl_stream_t stream)
 {
+    if (noise_mode != QERL_AQN_NOISE_ADD && noise_mode != QERL_AQN_NOISE_MUL) return QERL_ERR_INVALID_ARG;
+    const int mult = noise_mode == QERL_AQN_NOISE_MUL ? 1 : 0;
     if (!gamma || M < 0 || H < 1 || !(eps >= 0.0f)) return QERL_ERR_INVALID_ARG;
     if (M == 0) return QERL_OK;  // x and y may be NULL for an empty batch
     if (!x || !y) return QERL_ERR_INVALID_ARG;
@@ -273,7 +284,7 @@ extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, con
             return QERL_ERR_CUDA;
         return launched(launch_k(aqn_rmsnorm_fused_kernel, dim3((unsigned)g), dim3(kFusedThreads), smem, s,
                                  g_chain.load() != 0, static_cast<const __nv_bfloat16 *>(x), M, H,
-                                 static_cast<const __nv_bfloat16 *>(gamma), eps, sigma, seed, step, layer_id,
+                                 static_cast<const __nv_bfloat16 *>(gamma), eps, sigma, seed, step, layer_id, mult,
                                  static_cast<__nv_bfloat16 *>(y)));
     }
     float *gscale = nullptr;
@@ -282,12 +293,20 @@ extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, con
         const int64_t n = (H + 3) / 4;
         QERL_TRY(launched(launch_k(aqn_noise_kernel, dim3((unsigned)((n + 63) / 64)), dim3(64), 0, s,
                                    g_chain.load() != 0, H, seed, step, layer_id,
-                                   static_cast<const __nv_bfloat16 *>(gamma), sigma, gscale, (float *)nullptr,
-                                   (uint64_t *)nullptr)));
+                                   static_cast<const __nv_bfloat16 *>(gamma), sigma, mult, gscale,
+                                   (float *)nullptr, (uint64_t *)nullptr)));
     }
     int64_t g = M;
     if (g > 8 * num_sms()) g = 8 * num_sms();
     return launched(launch_k(rmsnorm_kernel, dim3((unsigned)g), dim3(kNormThreads), 0, s, g_chain.load() != 0,
                              static_cast<const __nv_bfloat16 *>(x), M, H, (const float *)gscale,
                              static_cast<const __nv_bfloat16 *>(gamma), eps, static_cast<__nv_bfloat16 *>(y)));
+}
+
+extern "C" qerl_status qerl_aqn_rmsnorm(const void *x, int64_t M, int64_t H, const void *gamma, float eps,
+                                        float sigma, uint64_t seed, uint64_t step, uint32_t layer_id, void *y,
+                                        void *ws, size_t ws_bytes, qerl_stream_t stream)
+{
+    return qerl_aqn_rmsnorm_mode(x, M, H, gamma, eps, sigma, seed, step, layer_id, QERL_AQN_NOISE_ADD, y, ws,
+                                 ws_bytes, stream);
 }

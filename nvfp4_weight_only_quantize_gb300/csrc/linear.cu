@@ -938,8 +938,34 @@ qerl_status lora_down_rows(const __nv_bfloat16 *x, int64_t M, int64_t K, const D
 size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
 {
     const size_t simt = round256(size_t(M) * r * sizeof(float));
-    const size_t tc = tc_fwd_ws_bytes(M, N, K, r);
-    return simt > tc ? simt : tc;
+    return std::max(std::max(simt, tc_fwd_ws_bytes(M, N, K, r)), gemv_ws_bytes(M, N, K, r));
+}
+
+// The CUDA-core GEMV takes one or two tokens when selected.  Under AUTO it
+// takes single-token calls on weights of up to 24M values (13.5 MB), where its
+// lower fixed cost per call beats the tensor-core kernel; on larger weights
+// the tensor-core kernel streams faster (measured on Qwen2.5-7B shapes).
+constexpr int64_t kGemvAutoMaxWeights = int64_t(24) << 20;
+static bool use_gemv(const FwdArgs &a, bool grouped = false)
+{
+    const int algo = g_algo.load();
+    const bool auto_pick = algo == QERL_ALGO_AUTO && !grouped && a.M == 1 && a.N * a.K <= kGemvAutoMaxWeights;
+    return (algo == QERL_ALGO_GEMV || auto_pick) && gemv_applies(a.M, a.N, a.K, a.r);
+}
+
+// One forward: GEMV, tensor cores, or the CUDA-core GEMM, in that order of
+// preference among the paths the selection allows and that cover the shape.
+static qerl_status run_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s, bool grouped = false)
+{
+    if (use_gemv(a, grouped)) {
+        const qerl_status st = gemv_fwd(a, ws, ws_bytes, s);
+        if (st != QERL_ERR_SHAPE) return st;
+    }
+    if (g_algo.load() != QERL_ALGO_SIMT) {
+        const qerl_status st = tc_linear_fwd(a, ws, ws_bytes, s);
+        if (st != QERL_ERR_SHAPE) return st;
+    }
+    return simt_fwd(a, ws, s);
 }
 
 size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r)
@@ -965,11 +991,7 @@ qerl_status linear_fwd_fixed_ws(const void *x, int64_t M, int64_t K, int64_t N, 
     const FwdArgs a{static_cast<const __nv_bfloat16 *>(x), M, K, N, codes, scales, tensor_scale,
                     static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), r,
                     lora_scale, static_cast<__nv_bfloat16 *>(y), t_out};
-    if (g_algo.load() != QERL_ALGO_SIMT) {
-        const qerl_status st = tc_linear_fwd(a, static_cast<char *>(ws), ws_cap, s);
-        if (st != QERL_ERR_SHAPE) return st;
-    }
-    return simt_fwd(a, static_cast<char *>(ws), s);
+    return run_fwd(a, static_cast<char *>(ws), ws_cap, s);
 }
 
 }  // namespace qerl
@@ -978,7 +1000,8 @@ using namespace qerl;
 
 extern "C" qerl_status qerl_set_linear_algo(int algo)
 {
-    if (algo != QERL_ALGO_AUTO && algo != QERL_ALGO_SIMT && algo != QERL_ALGO_TCGEN05) return QERL_ERR_INVALID_ARG;
+    if (algo != QERL_ALGO_AUTO && algo != QERL_ALGO_SIMT && algo != QERL_ALGO_TCGEN05 && algo != QERL_ALGO_GEMV)
+        return QERL_ERR_INVALID_ARG;
     g_algo.store(algo);
     return QERL_OK;
 }
@@ -998,12 +1021,7 @@ qerl_status fwd_entry(const void *x, int64_t M, int64_t K, int64_t N, const uint
     const FwdArgs a{static_cast<const __nv_bfloat16 *>(x), M, K, N, codes, scales, tensor_scale,
                     static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), r,
                     lora_scale, static_cast<__nv_bfloat16 *>(y), t_out, packed};
-    cudaStream_t s = as_cuda(stream);
-    if (g_algo.load() != QERL_ALGO_SIMT) {
-        const qerl_status st = tc_linear_fwd(a, static_cast<char *>(ws), ws_bytes, s);
-        if (st != QERL_ERR_SHAPE) return st;
-    }
-    return simt_fwd(a, static_cast<char *>(ws), s);
+    return run_fwd(a, static_cast<char *>(ws), ws_bytes, as_cuda(stream));
 }
 
 qerl_status bwd_entry(const void *dy, const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes,
@@ -1112,16 +1130,16 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_grouped(const void *x, int64_t
     }
     cudaStream_t s = as_cuda(stream);
     char *w = static_cast<char *>(ws);
-    if (g_algo.load() != QERL_ALGO_SIMT && n_groups > 1 && n_groups <= 3) {
+    // One tensor-core launch for all groups where it applies (AUTO keeps it at
+    // one token too: one launch beats a GEMV per group); a GEMV per group when
+    // the GEMV is selected.
+    bool gemv = true;
+    for (int g = 0; g < n_groups; ++g) gemv = gemv && use_gemv(a[g], true);
+    if (!gemv && g_algo.load() != QERL_ALGO_SIMT && n_groups > 1 && n_groups <= 3) {
         const qerl_status st = tc_fwd_groups(a, n_groups, w, ws_bytes, s);
         if (st != QERL_ERR_SHAPE) return st;
     }
-    for (int g = 0; g < n_groups; ++g) {  // one group after the other
-        qerl_status st = QERL_ERR_SHAPE;
-        if (g_algo.load() != QERL_ALGO_SIMT) st = tc_linear_fwd(a[g], w, ws_bytes, s);
-        if (st == QERL_ERR_SHAPE) st = simt_fwd(a[g], w, s);
-        QERL_TRY(st);
-    }
+    for (int g = 0; g < n_groups; ++g) QERL_TRY(run_fwd(a[g], w, ws_bytes, s, true));  // one group after the other
     return QERL_OK;
 }
 

@@ -46,6 +46,17 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
 // G (<= 3) linears sharing x, M, K, r, lora_scale and layout in one launch.
 qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, cudaStream_t s);
 size_t tc_fwd_groups_ws_bytes(int64_t M, const int64_t *N, int G, int64_t K, int r);
+// t = x A^T (FP32 [M, r] to `t`) and u = bf16(s t / (s_t 2^c)) ([M, r_pad],
+// zero past r; r_pad even) by the CUDA-core down-projection kernel, for
+// M <= 64 and K % 8 == 0.
+qerl_status lora_down_small(const FwdArgs &a, int r_pad, float *t, __nv_bfloat16 *u, bool chain, cudaStream_t s);
+
+// CUDA-core GEMV path (gemv.cu) for one or two tokens: QERL_ERR_SHAPE, having
+// launched nothing, when it does not cover the call (M > 2, K % 32 != 0, r >
+// 256, or x too large for shared memory).
+bool gemv_applies(int64_t M, int64_t N, int64_t K, int r);
+size_t gemv_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+qerl_status gemv_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s);
 
 inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 

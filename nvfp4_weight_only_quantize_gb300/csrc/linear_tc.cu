@@ -436,9 +436,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
             const uint32_t sround = (uint32_t)(j / C::S);
             const bool main_stage = j < main_stages;
             const int g = (j * SPS) / GK, rs = g % C::R;  // raw stage of a main stage
-            // Stage free first: the MMA is then past stage j - S, so every raw stage
-            // up to g - R has landed and the raw_full parity below cannot alias.
-            if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&stage_empty[s], (sround - 1) & 1u))) break;
+            // The raw stage first: its codes and scales are read, and the first
+            // k-step dequantized, while the MMA may still be reading this A slot.
+            // Parity: raw group g - R went through this slot before g, and this
+            // group consumed it at its stage j - R * GK / SPS, so that phase has
+            // completed and the raw_full parity below cannot alias.
             if (main_stage && !__all_sync(0xFFFFFFFFu, wait(&raw_full[rs], (uint32_t)(g / C::R) & 1u))) break;
             const int nsub = min(SPS, n_steps - j * SPS);
             // A main stage reads all of its codes and scales first (every load in
@@ -460,26 +462,33 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                     scw[sub] = *reinterpret_cast<const uint32_t *>(rb + RAW_CODES + row * 16 + q * 4);
                 }
             }
+            // k-step `sub` of a main stage -> 32 bf16 pairs of row `row`
+            auto dequant_step = [&](int sub, uint32_t (&out)[32]) {
+                const uint4 c0 = cw[2 * sub], c1 = cw[2 * sub + 1];
+                const uint32_t sc = scw[sub];
+                const uint32_t f0 = scale_factor_bf16x2(sc << 20, pow2);
+                const uint32_t f1 = scale_factor_bf16x2(sc << 12, pow2);
+                const uint32_t f2 = scale_factor_bf16x2(sc << 4, pow2);
+                const uint32_t f3 = scale_factor_bf16x2(sc >> 4, pow2);
+                dequant_word<PACKED>(c0.x, f0, out + 0);
+                dequant_word<PACKED>(c0.y, f0, out + 4);
+                dequant_word<PACKED>(c0.z, f1, out + 8);
+                dequant_word<PACKED>(c0.w, f1, out + 12);
+                dequant_word<PACKED>(c1.x, f2, out + 16);
+                dequant_word<PACKED>(c1.y, f2, out + 20);
+                dequant_word<PACKED>(c1.z, f3, out + 24);
+                dequant_word<PACKED>(c1.w, f3, out + 28);
+            };
+            uint32_t out[32];
+            if (main_stage) dequant_step(0, out);
+            // Then the A slot: free once the MMA is past stage j - S.
+            if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&stage_empty[s], (sround - 1) & 1u))) break;
 #pragma unroll
             for (int sub = 0; sub < SPS; ++sub) {
                 if (sub >= nsub) break;
                 const int i = j * SPS + sub;
-                uint32_t out[32];
                 if (main_stage) {
-                    const uint4 c0 = cw[2 * sub], c1 = cw[2 * sub + 1];
-                    const uint32_t sc = scw[sub];
-                    const uint32_t f0 = scale_factor_bf16x2(sc << 20, pow2);
-                    const uint32_t f1 = scale_factor_bf16x2(sc << 12, pow2);
-                    const uint32_t f2 = scale_factor_bf16x2(sc << 4, pow2);
-                    const uint32_t f3 = scale_factor_bf16x2(sc >> 4, pow2);
-                    dequant_word<PACKED>(c0.x, f0, out + 0);
-                    dequant_word<PACKED>(c0.y, f0, out + 4);
-                    dequant_word<PACKED>(c0.z, f1, out + 8);
-                    dequant_word<PACKED>(c0.w, f1, out + 12);
-                    dequant_word<PACKED>(c1.x, f2, out + 16);
-                    dequant_word<PACKED>(c1.y, f2, out + 20);
-                    dequant_word<PACKED>(c1.z, f3, out + 24);
-                    dequant_word<PACKED>(c1.w, f3, out + 28);
+                    if (sub > 0) dequant_step(sub, out);
                 } else {
                     // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
                     // (Chained: B may be written by work before this call.)
@@ -1007,6 +1016,15 @@ size_t tc_fwd_groups_ws_bytes(int64_t M, const int64_t *N, int G, int64_t K, int
     for (int g = 0; g < G; ++g)
         if (!tc_fwd_applies(M, N[g], K, r)) return 0;
     return plan_fwd(M, N, G, K, r).total;
+}
+
+qerl_status lora_down_small(const FwdArgs &a, int r_pad, float *t, __nv_bfloat16 *u, bool chain, cudaStream_t s)
+{
+    if (a.M < 1 || a.M > 64 || a.K % 8 != 0 || r_pad < a.r || r_pad % 2 != 0) return QERL_ERR_SHAPE;
+    constexpr int MB = 4, JB = 2;
+    const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (r_pad / JB));
+    return launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x, a.A,
+                             (int)a.M, (int)a.K, a.r, r_pad, a.lora_scale, a.tensor_scale, t, u));
 }
 
 qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s)

@@ -61,8 +61,11 @@ def test_argument_errors_return_before_any_launch(L):
     # AQN
     assert L.qerl_aqn_rmsnorm(fake, 4, 0, fake, 1e-6, 0.0, 0, 0, 0, fake, ws, 1 << 20, None) == 1
     assert L.qerl_aqn_rmsnorm(fake, 4, 64, fake, 1e-6, 0.1, 0, 0, 0, fake, None, 0, None) == 8
+    assert L.qerl_aqn_rmsnorm_mode(fake, 4, 64, fake, 1e-6, 0.1, 0, 0, 0, 2, fake, ws, 1 << 20, None) == 1
+    assert L.qerl_aqn_rmsnorm_mode(fake, 4, 64, fake, 1e-6, 0.1, 0, 0, 0, 1, fake, None, 0, None) == 8
     assert L.qerl_aqn_noise(0, 0, 0, 0, fake, None, None) == 1
     assert L.qerl_set_linear_algo(9) == 1
+    assert L.qerl_set_linear_algo(4) == 1
 
 
 def test_grouped_argument_errors_return_before_any_launch(L):

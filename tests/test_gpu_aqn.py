@@ -45,3 +45,27 @@ def test_rmsnorm_empty_batch():
     g = synth.norm_gamma(64, 1).cuda()
     y = q.qerl_aqn_rmsnorm(x, g, 1e-6, 0.1, 0, 0, 0)
     assert y.shape == (0, 64)
+
+
+@pytest.mark.parametrize("M,H,sigma", [(1, 3584, 1e-2), (64, 3584, 5e-2), (3, 100, 0.05), (2, 20000, 1e-2)])
+def test_rmsnorm_multiplicative_noise_parity(M, H, sigma):
+    """The multiplicative reading, gamma (1 + sigma z), through the one-launch
+    path (H <= 16384) and the two-kernel path (H = 20000); the additive mode
+    of the same entry point equals qerl_aqn_rmsnorm bit for bit."""
+    x = synth.activations(M, H, 5 * M + H).cuda()
+    g = synth.norm_gamma(H, H + 3).cuda()
+    y = q.qerl_aqn_rmsnorm(x, g, 1e-6, sigma, seed=9, step=4, layer_id=1, noise_mode=q.AQN_NOISE_MUL)
+    ref = oracle.aqn_rmsnorm(synth.bits(x), synth.bits(g), 1e-6, sigma, 9, 4, 1, multiplicative=True)
+    assert_rel_rms(f64(y), ref, NORM_TOL, "aqn_rmsnorm multiplicative", bf16_out=True)
+    ya = q.qerl_aqn_rmsnorm(x, g, 1e-6, sigma, seed=9, step=4, layer_id=1, noise_mode=q.AQN_NOISE_ADD)
+    yd = q.qerl_aqn_rmsnorm(x, g, 1e-6, sigma, seed=9, step=4, layer_id=1)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yd)
+    assert not torch.equal(ya, y)
+
+
+def test_rmsnorm_mode_rejects_unknown_mode():
+    x = torch.zeros(1, 16, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(q.QerlError):
+        q.qerl_aqn_rmsnorm(x, g, 1e-6, 0.1, seed=1, step=1, layer_id=1, noise_mode=2)
