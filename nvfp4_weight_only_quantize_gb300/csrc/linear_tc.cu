@@ -77,6 +77,9 @@ struct Cfg {
     // only after the MMA that read it completed, a ~2 us round trip.
     static constexpr int XS = FUSED ? 3 : (BN >= 128 ? 2 : 4);
     static constexpr int R = 4;  // raw (code+scale) stages
+    // k-steps of a main stage dequantized into registers before its A slot is
+    // free (the rest after): they come off the slot-reuse round trip.
+    static constexpr int EARLY = 2;
     static_assert(GK % SPS == 0 && GK / SPS <= DQG, "each group has at most one stage per raw stage");
     static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
     static_assert(R * GK >= S * SPS, "raw ring deep enough for parity-safe waits");
@@ -479,16 +482,26 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                 dequant_word<PACKED>(c1.z, f3, out + 24);
                 dequant_word<PACKED>(c1.w, f3, out + 28);
             };
-            uint32_t out[32];
-            if (main_stage) dequant_step(0, out);
+            constexpr int EARLY = C::EARLY < SPS ? C::EARLY : SPS;
+            uint32_t early[EARLY][32];
+            if (main_stage) {
+#pragma unroll
+                for (int e = 0; e < EARLY; ++e) dequant_step(e, early[e]);
+            }
             // Then the A slot: free once the MMA is past stage j - S.
             if (sround > 0 && !__all_sync(0xFFFFFFFFu, wait(&stage_empty[s], (sround - 1) & 1u))) break;
 #pragma unroll
             for (int sub = 0; sub < SPS; ++sub) {
                 if (sub >= nsub) break;
                 const int i = j * SPS + sub;
+                const uint32_t taddr = trow + (uint32_t)(C::A_COL0 + s * 32 * SPS + sub * 32);
+                if (main_stage && sub < EARLY) {
+                    tmem_st32(taddr, early[sub]);
+                    continue;
+                }
+                uint32_t out[32];
                 if (main_stage) {
-                    if (sub > 0) dequant_step(sub, out);
+                    dequant_step(sub, out);
                 } else {
                     // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
                     // (Chained: B may be written by work before this call.)
@@ -515,7 +528,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                     }
                 }
                 // row `row` of the step's A tile: TMEM lane `row`, 32 columns of bf16 pairs
-                tmem_st32(trow + (uint32_t)(C::A_COL0 + s * 32 * SPS + sub * 32), out);
+                tmem_st32(taddr, out);
             }
             if (main_stage) {
                 __syncwarp();
