@@ -4,7 +4,8 @@
 // Gaussian noise via the normalization layer with an exponential decay
 // schedule; dataforcee "QERL: NVFP4-intensive learning" AQN paragraph: the noise
 // lives in the norm's scale parameters.  So the norm uses gamma + sigma * z with
-// one z[H] ~ N(0, 1) per (seed, step, layer), shared by every token.
+// one z[H] ~ N(0, 1) per (seed, step, layer), shared by every token; the other
+// reading of that sentence, gamma (1 + sigma z), is the multiplicative mode.
 //
 // One kernel for hidden sizes up to kFusedMaxH: every CTA draws the noisy scale
 // vector gamma + sigma z into shared memory (Philox4x64-10, Box-Muller in FP32)
@@ -62,13 +63,14 @@ __device__ __forceinline__ void noise4(uint64_t i, uint64_t seed, uint64_t step,
     box_muller(w[2], w[3], z[2], z[3]);
 }
 
-// One thread per Philox block: channels 4i .. 4i+3.  Writes any of z_out /
-// raw_out / scale_out given.
 // Noisy scale of channel c: gamma + sigma z (additive) or gamma (1 + sigma z).
 __device__ __forceinline__ float noisy_scale(float g, float sigma, float z, int mult)
 {
     return mult ? g * (1.0f + sigma * z) : g + sigma * z;
 }
+
+// One thread per Philox block: channels 4i .. 4i+3.  Writes any of z_out /
+// raw_out / scale_out given.
 
 __global__ void aqn_noise_kernel(int64_t H, uint64_t seed, uint64_t step, uint32_t layer,
                                  const __nv_bfloat16 *__restrict__ gamma, float sigma, int mult,
@@ -185,17 +187,26 @@ __global__ void __launch_bounds__(kFusedThreads)
     extern __shared__ float gs[];  // [H]
     __shared__ float red[32];
     pdl_trigger();
-    pdl_wait();  // x, gamma and y follow the preceding work when the launch is chained
+    // The draws need no input: z goes to shared memory before the wait for the
+    // preceding work (x, gamma and y follow it when the launch is chained).
     const int64_t nb = (H + 3) / 4;
     const bool noisy = sigma != 0.0f;
-    for (int64_t i = threadIdx.x; i < nb; i += blockDim.x) {
-        float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        uint64_t w[4];
-        if (noisy) noise4((uint64_t)i, seed, step, layer, z, w);
+    if (noisy) {
+        for (int64_t i = threadIdx.x; i < nb; i += blockDim.x) {
+            float z[4];
+            uint64_t w[4];
+            noise4((uint64_t)i, seed, step, layer, z, w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (4 * i + e < H) gs[4 * i + e] = z[e];
+        }
+    }
+    pdl_wait();
+    for (int64_t i = threadIdx.x; i < nb; i += blockDim.x) {  // the same channels as drawn above
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int64_t c = 4 * i + e;
-            if (c < H) gs[c] = noisy_scale(bf16f(gamma[c]), sigma, z[e], mult);
+            if (c < H) gs[c] = noisy ? noisy_scale(bf16f(gamma[c]), sigma, gs[c], mult) : bf16f(gamma[c]);
         }
     }
     __syncthreads();
