@@ -89,7 +89,7 @@ struct Plan {
     int *phase_cnt;            // [n_phases] (zero between launches)
     int *tile_cnt;             // per phase tile counters (zero between launches)
     int *exit_cnt;             // (zero between launches)
-    float *partials;           // [slots][128][64]
+    float *partials;           // [slots][64 tokens][128 rows]
     unsigned int *err;
     unsigned long long timeout_ns;
 };

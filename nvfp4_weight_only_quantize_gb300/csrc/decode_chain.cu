@@ -641,10 +641,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             if (J.nparts > 1) {
-                // this part's partial tile; the last part of the tile to finish sums them
-                float *part = P.partials + (size_t)J.slot * (TILE_N * BN) + (size_t)row * BN;
+                // this part's partial tile [token][row] (a warp's 32 rows of one token
+                // are 128 contiguous bytes); the last part of the tile to finish sums them
+                float *part = P.partials + (size_t)J.slot * (TILE_N * BN) + row;
 #pragma unroll
-                for (int c = 0; c < BN; c += 4) __stcg(reinterpret_cast<float4 *>(part + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+                for (int c = 0; c < BN; ++c) __stcg(part + (size_t)c * TILE_N, v[c]);
                 __threadfence();
                 named_bar_sync(BAR_EPI, EPI_THREADS);
                 if (et == 0) {
@@ -656,19 +657,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 named_bar_sync(BAR_EPI, EPI_THREADS);
                 if (!last) continue;
                 __threadfence();
-                const float *p0 = P.partials + (size_t)(J.slot - J.part) * (TILE_N * BN) + (size_t)row * BN;
+                const float *p0 = P.partials + (size_t)(J.slot - J.part) * (TILE_N * BN) + row;
 #pragma unroll
                 for (int c = 0; c < BN; ++c) v[c] = 0.0f;
-                for (int pi = 0; pi < J.nparts; ++pi) {
+                for (int pi = 0; pi < J.nparts; ++pi) {  // in part order (deterministic)
                     const float *pp = p0 + (size_t)pi * (TILE_N * BN);
+                    float w[BN];  // every load of the part in flight before the adds
 #pragma unroll
-                    for (int c = 0; c < BN; c += 4) {
-                        const float4 w = __ldcg(reinterpret_cast<const float4 *>(pp + c));
-                        v[c] += w.x;
-                        v[c + 1] += w.y;
-                        v[c + 2] += w.z;
-                        v[c + 3] += w.w;
-                    }
+                    for (int c = 0; c < BN; ++c) w[c] = __ldcg(pp + (size_t)c * TILE_N);
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) v[c] += w[c];
                 }
                 if (et == 0) P.tile_cnt[L.tile0 + J.tile] = 0;  // clean for the next launch
             }
