@@ -172,12 +172,16 @@ class DecodeLayer:
         return dict(outs=outs, h1=torch.empty(M, wl.hidden, dtype=torch.bfloat16, device=device),
                     h2=torch.empty(M, wl.hidden, dtype=torch.bfloat16, device=device),
                     ws=torch.empty(max(ws_lin, 1), dtype=torch.uint8, device=device),
+                    ws_side=torch.empty(max(ws_lin, 1), dtype=torch.uint8, device=device),
+                    side=torch.cuda.Stream(device=device),
                     ws_norm=self.q.workspace(self.q.OP_AQN_RMSNORM, M, 0, wl.hidden, 0, device))
 
     def step(self, copy, x, attn, buf, sigma, step_idx):
         """One decoder layer: norm -> q|k|v (one grouped call) -> o -> norm ->
-        gate -> up -> down.  Attention and SwiGLU are not part
-        of this step (synthetic attention output; down reads up's output)."""
+        gate and up (both read the norm's output: up runs on a second stream
+        with its own workspace, joined before down) -> down.  Attention and
+        SwiGLU are not part of this step (synthetic attention output; down
+        reads up's output)."""
         q = self.q
         lins, gammas = self.copies[copy]
         by = {l[0]: l for l in lins}
@@ -189,19 +193,25 @@ class DecodeLayer:
             q.qerl_nvfp4_lora_linear_fwd_grouped(xin, gs, s, packed=self.packed, ys=[o[n] for n in names],
                                                  ws=buf["ws"])
 
-        def single(name, xin):
+        def single(name, xin, ws="ws"):
             _, N, K, codes, scales, ts, A, B = by[name]
-            self.fwd(xin, codes, scales, ts, A, B, s, y=o[name], ws=buf["ws"])
+            self.fwd(xin, codes, scales, ts, A, B, s, y=o[name], ws=buf[ws])
 
         q.qerl_aqn_rmsnorm(x, gammas[0], 1e-6, sigma, 1, step_idx, 2 * copy, y=buf["h1"], ws=buf["ws_norm"])
         group(("q_proj", "k_proj", "v_proj"), buf["h1"])
         single("o_proj", attn)
         q.qerl_aqn_rmsnorm(o["o_proj"], gammas[1], 1e-6, sigma, 1, step_idx, 2 * copy + 1, y=buf["h2"],
                            ws=buf["ws_norm"])
-        # gate and up stay separate calls: grouped they need two waves of
-        # one-tile CTAs over the SMs, which measured slower than two launches
+        # gate and up stay separate calls (grouped they need two waves of
+        # one-tile CTAs over the SMs, which measured slower); up runs on a
+        # second stream, so its CTAs take each SM as gate's leave it instead of
+        # waiting for the whole of gate
+        cur, side = torch.cuda.current_stream(), buf["side"]
+        side.wait_stream(cur)
         single("gate_proj", buf["h2"])
-        single("up_proj", buf["h2"])
+        with torch.cuda.stream(side):
+            single("up_proj", buf["h2"], ws="ws_side")
+        cur.wait_stream(side)
         single("down_proj", o["up_proj"])
         return o["down_proj"]
 
@@ -332,7 +342,8 @@ def run_ours(args, rank, world, local_rank):
                    "layer_copies_rotated": n_copies,
                    "l2": f"inputs larger than L2: {n_copies} rotating layer copies, "
                          f"{n_copies * per_copy / 2**20:.0f} MiB NVFP4 > 129 MiB L2",
-                   "launch": "one CUDA graph per step (per weight copy); q|k|v as one grouped call",
+                   "launch": "one CUDA graph per step (per weight copy); q|k|v as one grouped call; up_proj on a "
+                             "second stream beside gate_proj",
                    "codes": args.codes + " layout (packed once when the weights are loaded)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tokens_per_s": round(M * args.steps * world / max_secs, 1),
