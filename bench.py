@@ -657,6 +657,42 @@ def other_rows(dev, only=None, profile=False):
                                         "bytes": "2 B read + 0.5625 B written per weight"}
         del Ws, outs
     del W
+    # the decoder chain on one Qwen2.5-7B layer, M = 64, r = 32 (a profiling row:
+    # its numbers are also in the decode rows)
+    if only == "chain":
+        wl = synth.WORKLOADS[1]
+        M, H, I = 64, wl.hidden, 18944
+        lay = _chain_layers(q, synth, 2, M, H, H, 512, I, wl.r, 1, dev)
+        xc = synth.activations(M, H, 5, dev)
+        yc = torch.empty_like(xc)
+        plans = [q.DecoderChain([lay[c]], M, H, H, 512, I, wl.r, wl.lora_scale, 1e-6, xc, yc) for c in range(2)]
+        sigma = q.qerl_aqn_sigma(0, 1000, wl.sigma[0], wl.sigma[1], 10)
+        sec = timed(lambda: [p_.run(sigma, 1, 0) for p_ in plans], 5) / 2
+        rows["chain_layer"] = {"workload": "qwen2.5-7b decoder layer through the decoder-chain kernel, M=64, r=32",
+                               "us": round(sec * 1e6, 1), "GBps": round(layer_bytes(wl) / sec / 1e9, 1)}
+        del plans, lay
+    # the CUDA-core GEMV on one token: Qwen2.5-7B o_proj 3584 x 3584, 8 rotating
+    # copies (a profiling row: its numbers are also in the decode rows)
+    if only == "gemv":
+        N, K, r, nc = 3584, 3584, 32, 8
+        wts = []
+        for c in range(nc):
+            W = synth.weight(N, K, 40 + c, dev)
+            cs = q.qerl_nvfp4_quantize(W)
+            del W
+            q.qerl_nvfp4_pack_codes(cs[0], out=cs[0])
+            wts.append((*cs, synth.lora_A(r, K, 50 + c, dev), synth.lora_B(N, r, 60 + c, dev)))
+        x1 = synth.activations(1, K, 70, dev)
+        y1 = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
+        ws1 = q.workspace(q.OP_LINEAR_FWD, 1, N, K, r, dev)
+        q.set_linear_algo(q.ALGO_GEMV)
+        try:
+            sec = timed(lambda: [q.qerl_nvfp4_lora_linear_fwd_packed(x1, *w_, 2.0, y=y1, ws=ws1) for w_ in wts], 5) / nc
+        finally:
+            q.set_linear_algo(q.ALGO_AUTO)
+        rows["gemv_one_token"] = {"workload": f"qwen2.5-7b o_proj {N}x{K}, M=1, r={r}", "us": round(sec * 1e6, 2),
+                                  "GBps": round(linear_bytes(N, K, r) / sec / 1e9, 1)}
+        del wts
     # f3: the forwards with an MXFP4 weight and with FP32 LoRA adapters (CUDA-core
     # GEMM), beside the NVFP4 forward, on qwen2.5-7b gate_proj at M = 8, r = 32
     if want("f3"):
@@ -896,7 +932,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the quantize/norm/prefill/backward lines")
-    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5", "f2", "f3"],
+    ap.add_argument("--profile-row", choices=["a1", "a2", "a4", "a5", "f2", "f3", "chain", "gemv"],
                     help="run only that row's measurement, its timed launches bracketed by "
                          "cudaProfilerStart/Stop (for ncu --profile-from-start off), and print it")
     ap.add_argument("--codes", default="packed", choices=["packed", "standard"],
