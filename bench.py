@@ -310,22 +310,53 @@ def run_ours(args, rank, world, local_rank):
         us = _time_graph(g, reps) / (reps * n_copies) * 1e6
         per_linear[name] = {"us": round(us, 2), "GBps": round(linear_bytes(N, K, wl.r) / us / 1e3, 1)}
 
-    # --- end to end through the public API with host buffers
+    # --- end to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory and reads its output back.  Two buffer
+    # sets alternate, so that step i + 1's inputs are copied in (one copy
+    # stream) and step i - 1's output is read back (another) while step i
+    # computes; a set is reused only after the step that last used it finished.
     xh = x.cpu().pin_memory()
     ah = attn.cpu().pin_memory()
-    yh = torch.empty(M, wl.hidden, dtype=torch.bfloat16).pin_memory()
-    out = buf["outs"]["down_proj"]
+    sets = []
+    for p_ in range(2):
+        bset = buf if p_ == 0 else layer.buffers(M, dev)
+        xs = x if p_ == 0 else torch.empty_like(x)
+        ats = attn if p_ == 0 else torch.empty_like(attn)
+        gs = graphs if p_ == 0 else [_graph(lambda c=c, b_=bset, x_=xs, a_=ats: layer.step(c, x_, a_, b_, sigma, c))
+                                     for c in range(n_copies)]
+        sets.append(dict(x=xs, attn=ats, graphs=gs, out=bset["outs"]["down_proj"],
+                         yh=torch.empty(M, wl.hidden, dtype=torch.bfloat16).pin_memory(),
+                         loaded=torch.cuda.Event(), done=torch.cuda.Event(), read=torch.cuda.Event()))
+    comp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e0.record(comp)
+    h2d.wait_stream(comp)
+    d2h.wait_stream(comp)
     for i in range(args.steps):
-        x.copy_(xh, non_blocking=True)
-        attn.copy_(ah, non_blocking=True)
-        graphs[i % n_copies].replay()
-        yh.copy_(out, non_blocking=True)
-    e1.record()
+        st_ = sets[i % 2]
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(st_["done"])  # the set's previous step has finished
+            st_["x"].copy_(xh, non_blocking=True)
+            st_["attn"].copy_(ah, non_blocking=True)
+            st_["loaded"].record(h2d)
+        comp.wait_event(st_["loaded"])
+        if i >= 2:
+            comp.wait_event(st_["read"])  # the set's previous output has been read back
+        st_["graphs"][i % n_copies].replay()
+        st_["done"].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(st_["done"])
+            st_["yh"].copy_(st_["out"], non_blocking=True)
+            st_["read"].record(d2h)
+    comp.wait_stream(d2h)
+    comp.wait_stream(h2d)
+    e1.record(comp)
     torch.cuda.synchronize()
+    assert q.get_error() == 0
     e2e_secs, e2e_units = combine_ranks(e0.elapsed_time(e1) / 1e3, layer.bytes_per_step * args.steps)
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
