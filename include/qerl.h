@@ -129,8 +129,10 @@ qerl_status qerl_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales,
  *   B      (device) bf16 [N, r]        y (device) out bf16 [M, N]
  *   t_out  (device) optional out float [M, r] = x * A^T (for the backward); NULL ok
  *   Accumulation is FP32; the result is rounded to bf16 once.  1 <= r <= 256,
- *   K % 16 == 0, M, N >= 1; x, A, B, y and the codes rows 16-byte aligned
- *   (K % 32 == 0 for the tensor-core path, else the CUDA-core path runs).
+ *   K % 16 == 0, M, N >= 1; x, A, B, y and the codes rows 16-byte aligned.
+ *   Kernels (see qerl_set_linear_algo): tcgen05 for K % 256 == 0; the CUDA-core
+ *   GEMV for single-token calls on small weights (K % 32 == 0); the CUDA-core
+ *   GEMM for the rest.  All compute the same result within rounding.
  *   ws (device) >= qerl_workspace_bytes(QERL_OP_LINEAR_FWD, M, N, K, r).
  */
 qerl_status qerl_nvfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
