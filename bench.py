@@ -590,7 +590,8 @@ def decode_rows(dev):
         cross[M] = row
     out["c1_crossover_gate_proj"] = {"workload": f"qwen2.5-7b gate_proj {N}x{K}, {n_copies} rotating copies",
                                      "by_M": cross,
-                                     "auto": "AUTO takes the GEMV at M <= 2 and the tensor-core path above"}
+                                     "auto": "AUTO takes the GEMV for single-token calls on weights up to 24M values (not this "
+                                             "one) and the tensor-core path otherwise"}
     del layer
     torch.cuda.empty_cache()
     # the decoder-chain kernel on one 7B layer (norms, residuals and SwiGLU fused), 4 rotating layers
