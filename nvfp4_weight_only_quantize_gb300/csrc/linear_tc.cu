@@ -10,19 +10,21 @@
 // The exponent offset c is derived from s_t so that w'' and u are normal bf16
 // numbers and ysc is finite (see tc_exponent_offset).
 //
-// Warp roles (352 threads, one CTA per SM):
-//   warps 0-7  dequantize, as two groups of four warps taking alternate stages:
-//              packed codes + block scales (smem) -> bf16 A tile in the
-//              128-byte-swizzled K-major layout; warps 0-3 also run the
-//              epilogue (TMEM -> registers -> smem -> y, or split-K partials).
-//   warp 8     TMA producer of the packed codes and block scales, 4 k-steps
+// Warp roles (one CTA per SM; 352 threads for token tiles up to 128, 608 for
+// 256-token tiles):
+//   warps 0..4G-1  dequantize, as G = 2 (or 4) groups of four warps taking the
+//              stages in turn: packed codes + block scales (smem) -> bf16 A
+//              tile in TMEM; warps 0-3 also run the epilogue (TMEM ->
+//              registers -> smem -> y, or split-K partials).
+//   warp 4G    TMA producer of the packed codes and block scales, 4 k-steps
 //              (256 k: 128 code bytes per row, full lines) per raw stage.
-//   warp 9     TMA producer of the token tile (x, then u for the LoRA steps).
-//   warp 10    allocates TMEM and issues tcgen05.mma and the commits (one
+//   warp 4G+1  TMA producer of the token tile (x, then u for the LoRA steps).
+//   warp 4G+2  allocates TMEM and issues tcgen05.mma and the commits (one
 //              elected lane of the converged warp).
 // A pipeline stage is SPS k-steps: 4 (one raw stage) for token tiles up to 128,
-// 2 for 256-token tiles (their token stages are larger); each stage costs every
-// role mbarrier round trips of ~100+ cycles, so stages are made long.
+// 1 for 256-token tiles (their token stages are four times larger, and one
+// k-step of 256 tokens is already 512 MMA cycles); each stage costs every role
+// mbarrier round trips of ~100+ cycles, so decode stages are made long.
 // Every mbarrier wait is bounded by a deadline; on expiry the CTA latches
 // QERL_ERR_TIMEOUT, every role leaves its loop, in-flight copies and MMAs are
 // drained (bounded), TMEM is freed and the CTA exits.
@@ -60,29 +62,35 @@ constexpr int FUSED_R = 32;  // LoRA rows loaded per k-step in fused mode
 template <int BN, bool FUSED = false>
 struct Cfg {
     // Dequant groups of four warps; group g takes the stages j = g (mod DQG).
-    static constexpr int DQG = 2;
+    // Two for token tiles up to 128, four for 256-token tiles (one k-step per
+    // stage there: every group takes one k-step of each raw stage).
+    static constexpr int DQG = BN >= 256 ? 4 : 2;
     static constexpr int NUM_DQ_WARPS = DQG * DQ_GROUP_WARPS;
     static constexpr int WARP_RAW = NUM_DQ_WARPS, WARP_X = NUM_DQ_WARPS + 1, WARP_MMA = NUM_DQ_WARPS + 2;
     static constexpr int NUM_THREADS = (NUM_DQ_WARPS + 3) * 32;
-    // k-steps per pipeline stage (2 = 128 k, 4 = 256 k).
-    static constexpr int SPS = BN >= 256 ? 2 : 4;
+    // k-steps per pipeline stage (1 = 64 k, 4 = 256 k).
+    static constexpr int SPS = BN >= 256 ? 1 : 4;
     // A stage holds SPS k-steps of the dequantized weight tile (TMEM); at least
     // DQG of them, so a group never waits on a stage two mbarrier phases ahead
     // of the MMA (parity aliasing).  More stages than groups (where TMEM
     // allows): a group can fill a free stage while the MMA still reads the ones
     // filled before.
-    static constexpr int S = SPS == 4 ? 3 : 4;
+    static constexpr int S = SPS == 4 ? 3 : 8;
     static_assert(S >= DQG, "parity waits need at least one stage per dequant group");
     // Token-tile stages (smem), deeper than the A ring: a token slot is reloaded
-    // only after the MMA that read it completed, a ~2 us round trip.
-    static constexpr int XS = FUSED ? 3 : (BN >= 128 ? 2 : 4);
-    static constexpr int R = 4;  // raw (code+scale) stages
+    // only after the MMA that read it completed, a ~2 us round trip.  256-token
+    // tiles take five one-k-step stages (160 KB) beside two raw stages.
+    static constexpr int XS = BN >= 256 ? 5 : (FUSED ? 3 : (BN >= 128 ? 2 : 4));
+    static constexpr int R = BN >= 256 ? 2 : 4;  // raw (code+scale) stages
     // k-steps of a main stage dequantized into registers before its A slot is
     // free (the rest after): they come off the slot-reuse round trip.
     static constexpr int EARLY = 2;
     static_assert(GK % SPS == 0 && GK / SPS <= DQG, "each group has at most one stage per raw stage");
     static constexpr int RAW_CONSUMERS = (GK / SPS) * DQ_GROUP_WARPS;  // warps that read one raw stage
     static_assert(R * GK >= S * SPS, "raw ring deep enough for parity-safe waits");
+    // A group waits for a raw stage before its A slot: the slot's previous raw
+    // stage, R raw stages back, was then consumed by this same group.
+    static_assert((R * GK / SPS) % DQG == 0, "a raw slot's previous fill belongs to the waiting group");
     static constexpr int X_STEP = BN * BK * 2;
     static constexpr int X_STAGE = X_STEP * SPS;
     // fused: the LoRA A rows of each k-step (FUSED_R x 64 bf16, 128-byte rows)
