@@ -173,3 +173,17 @@ def test_deterministic(gemv):
     ys = [q.qerl_nvfp4_lora_linear_fwd(c.x, c.codes, c.scales, c.ts, c.A, c.B, c.s) for _ in range(3)]
     torch.cuda.synchronize()
     assert all(torch.equal(ys[0], y) for y in ys[1:])
+
+
+@pytest.mark.parametrize("M,K", [(1, 50944), (2, 25344), (2, 25600)])
+def test_shared_memory_limit(gemv, M, K):
+    """x staged in up to 200 KiB of shared memory: M * (K + r) * 4 bytes at the
+    limit (1 x 50944 and 2 x 25344 take the GEMV), and just past it for two
+    tokens (2 x 25600 falls back to the tensor-core kernel); every output
+    checked on a narrow weight."""
+    r = 16
+    c = LinearCase(M, K, 40, r, config=10, idx=K + M).quantize_gpu()
+    y = q.qerl_nvfp4_lora_linear_fwd(c.x, c.codes, c.scales, c.ts, c.A, c.B, c.s)
+    torch.cuda.synchronize()
+    assert q.get_error() == 0
+    _check(c, y)
