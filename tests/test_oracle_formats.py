@@ -35,8 +35,8 @@ def test_format_size_facts():
     # 4 bits per code + one 8-bit scale per block of 16 = 4.5 bits/value; ratios vs FP16/FP8.
     bits = 4 + 8 / int(G["block_size"])
     assert bits == float(G["bits_per_value"])
-    assert 16 / bits == pytest.approx(float(G["ratio_vs_fp16"]), abs=0.1)  # "~3.5x"
-    assert 8 / bits == pytest.approx(float(G["ratio_vs_fp8"]), abs=0.05)  # "~1.8x"
+    assert 16 / bits == pytest.approx(float(G["ratio_vs_fp16"]), abs=0.1)  # about 3.5 times
+    assert 8 / bits == pytest.approx(float(G["ratio_vs_fp8"]), abs=0.05)  # about 1.8 times
 
 
 def _threshold_code(q: float) -> int:

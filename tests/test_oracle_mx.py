@@ -20,6 +20,24 @@ def bf16_bits(a):
     return torch.tensor(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def test_block_of_32_shares_one_scale():
+    """The page's MXFP4 block size (golden fixture): a large value at position 31
+    sets the scale of positions 0..31 (so the small ones there round to zero),
+    while positions 32..63 get their own scale and keep their small values."""
+    from conftest import golden
+    bs = int(golden("nvfp4_format.txt")["mxfp4_block_size"])
+    w = np.full((1, 2 * bs), 0.1, np.float32)
+    w[0, bs - 1] = 100.0
+    rc, qc, qs = oracle.mxfp4_quantize(bf16_bits(w))
+    assert rc == 0 and qs.shape == (1, 2)
+    codes = np.zeros(2 * bs, np.int64)
+    codes[0::2] = qc[0] & 15
+    codes[1::2] = qc[0] >> 4
+    assert np.all(codes[:bs - 1] == 0) and codes[bs - 1] == 7
+    assert np.all(codes[bs:] != 0)
+    assert qs[0, 0] > qs[0, 1]
+
+
 def test_e8m0_decoder_every_byte():
     for b in range(255):
         assert oracle.e8m0_value(b) == math.ldexp(1.0, b - 127)
