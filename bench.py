@@ -725,35 +725,46 @@ def other_rows(dev, only=None, profile=False):
         rows["gemv_one_token"] = {"workload": f"qwen2.5-7b o_proj {N}x{K}, M=1, r={r}", "us": round(sec * 1e6, 2),
                                   "GBps": round(linear_bytes(N, K, r) / sec / 1e9, 1)}
         del wts
-    # f3: the forwards with an MXFP4 weight and with FP32 LoRA adapters (CUDA-core
-    # GEMM), beside the NVFP4 forward, on qwen2.5-7b gate_proj at M = 8, r = 32
+    # f3: the forwards with an MXFP4 weight and with FP32 LoRA adapters beside the
+    # NVFP4 forward, on qwen2.5-7b gate_proj at M = 8, r = 32: four weight copies
+    # rotated (above L2), on tcgen05 (the default selection) and, for context, on
+    # the CUDA-core GEMM
     if want("f3"):
-        N, K, M, r = 18944, 3584, 8, 32
-        W = synth.weight(N, K, 11, dev)
-        ncodes, nscales, nts = q.qerl_nvfp4_quantize(W)
-        mcodes, mscales = q.qerl_mxfp4_quantize(W)
-        del W
+        N, K, M, r, NC = 18944, 3584, 8, 32, 4
+        nv, mx = [], []
+        for c in range(NC):
+            W = synth.weight(N, K, 11 + 100 * c, dev)
+            nv.append(q.qerl_nvfp4_quantize(W))
+            mx.append(q.qerl_mxfp4_quantize(W))
+            del W
         x = synth.activations(M, K, 14, dev)
         A, B = synth.lora_A(r, K, 15, dev), synth.lora_B(N, r, 16, dev)
         Af, Bf = A.float(), B.float()
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         wsl = q.workspace(q.OP_LINEAR_FWD, M, N, K, r, dev)
-        arms = {"nvfp4_bf16_adapters": lambda: q.qerl_nvfp4_lora_linear_fwd(x, ncodes, nscales, nts, A, B, 2.0, y=y,
-                                                                            ws=wsl),
-                "nvfp4_fp32_adapters": lambda: q.qerl_nvfp4_lora_linear_fwd_f32ab(x, ncodes, nscales, nts, Af, Bf, 2.0,
-                                                                              y=y, ws=wsl),
-                "mxfp4_bf16_adapters": lambda: q.qerl_mxfp4_lora_linear_fwd(x, mcodes, mscales, A, B, 2.0, y=y,
-                                                                            ws=wsl)}
+        wsf = q.workspace(q.OP_LINEAR_FWD_F32AB, M, N, K, r, dev)
+        wsm = q.workspace(q.OP_MXFP4_FWD, M, N, K, r, dev)
+        arms = {
+            "nvfp4_bf16_adapters": lambda: [q.qerl_nvfp4_lora_linear_fwd(x, *w_, A, B, 2.0, y=y, ws=wsl) for w_ in nv],
+            "nvfp4_fp32_adapters": lambda: [q.qerl_nvfp4_lora_linear_fwd_f32ab(x, *w_, Af, Bf, 2.0, y=y, ws=wsf)
+                                            for w_ in nv],
+            "mxfp4_bf16_adapters": lambda: [q.qerl_mxfp4_lora_linear_fwd(x, *w_, A, B, 2.0, y=y, ws=wsm) for w_ in mx]}
         res = {}
         for name, fn in arms.items():
-            sec = timed(fn, 10)
+            sec = timed(fn, 10) / NC
             wbytes = N * K * (0.5 + (1 / 32 if name.startswith("mx") else 1 / 16))
             res[name] = {"us": round(sec * 1e6, 1), "weight_GBps": round(wbytes / sec / 1e9, 1)}
-        rows["f3_format_variants_fwd"] = {"workload": f"qwen2.5-7b gate_proj {N}x{K}, M={M}, r={r}",
-                                          "by_format": res,
-                                          "path": "NVFP4 with bf16 adapters on tcgen05; the FP32-adapter and MXFP4 "
-                                                  "forwards on the CUDA-core GEMM"}
-        del ncodes, nscales, nts, mcodes, mscales
+            if name != "nvfp4_bf16_adapters":
+                q.set_linear_algo(q.ALGO_SIMT)
+                res[name]["cuda_core_gemm_us"] = round(timed(fn, 2, warm=1) / NC * 1e6, 1)
+                q.set_linear_algo(q.ALGO_AUTO)
+        rows["f3_format_variants_fwd"] = {
+            "workload": f"qwen2.5-7b gate_proj {N}x{K}, M={M}, r={r}, {NC} weight copies rotated (above L2)",
+            "by_format": res,
+            "path": "tcgen05 for all three (MXFP4: scales written at one byte per 16 values each call, E8M0 factor "
+                    "in the dequantizer; FP32 adapters: LoRA term as three bf16 hi/lo products); "
+                    "cuda_core_gemm_us: the same call on the CUDA-core GEMM"}
+        del nv, mx
     # a2: decode and prefill norms
     for M, H, tag in ([(64, 3584, "decode M=64 H=3584"), (4096, 5120, "prefill M=4096 H=5120")] if want("a2") else []):
         x = synth.activations(M, H, 12, dev)

@@ -73,7 +73,9 @@ enum {
     QERL_OP_QUANTIZE = 0,
     QERL_OP_LINEAR_FWD = 1,
     QERL_OP_LINEAR_BWD = 2,
-    QERL_OP_AQN_RMSNORM = 3
+    QERL_OP_AQN_RMSNORM = 3,
+    QERL_OP_MXFP4_FWD = 4,        /* qerl_mxfp4_lora_linear_fwd */
+    QERL_OP_LINEAR_FWD_F32AB = 5  /* qerl_nvfp4_lora_linear_fwd_f32ab */
 };
 
 /* Linear algorithm selection (qerl_set_linear_algo); AUTO is the default.
@@ -335,7 +337,14 @@ float qerl_aqn_sigma(int64_t step, int64_t total_steps, float sigma_start, float
  * Format variants (bitsofall "QeRL: NVFP4-Quantized Reinforcement Learning",
  * "NVFP4" section, which sets NVFP4 against MXFP4, whose blocks are 32 values
  * with a power-of-two scale; and its LoRA paragraph, which keeps the adapters
- * in higher precision, e.g. FP32).  These run on CUDA cores.
+ * in higher precision, e.g. FP32).
+ *
+ * The two variant forwards run on the tcgen05 kernel of the NVFP4 forward
+ * when K % 256 == 0 and x, y, codes, scales, A, B (and t_out) are 16-byte
+ * aligned, unless qerl_set_linear_algo selected QERL_ALGO_SIMT; otherwise on
+ * the CUDA-core GEMM.  ws (device) >= qerl_workspace_bytes(QERL_OP_MXFP4_FWD
+ * or QERL_OP_LINEAR_FWD_F32AB, M, N, K, r) bytes, contents on entry ignored
+ * (QERL_ERR_WORKSPACE otherwise).
  *
  * MXFP4 quantizer: W (device) bf16 [N, K] (row stride ldw elements), K % 32 ==
  * 0 -> codes (device, 16-byte aligned) u8 [N, K/2] (element 2j in the low
@@ -351,16 +360,22 @@ qerl_status qerl_mxfp4_quantize(const void *W, int64_t N, int64_t K, int64_t ldw
 
 /* y = x w_hat^T + s (x A^T) B^T with an MXFP4 weight, w_hat = e2m1(code) *
  * 2^(scale byte - 127); x bf16 [M, K], A bf16 [r, K], B bf16 [N, r], y bf16
- * [M, N], t_out (optional) FP32 [M, r].  ws (device): M * r * 4 bytes (rounded
- * up to 256) unless t_out is given.  K % 32 == 0, 1 <= r <= 256. */
+ * [M, N], t_out (optional) FP32 [M, r].  K % 32 == 0, 1 <= r <= 256.
+ * Tensor-core path: each call first writes the scales into ws at one byte per
+ * 16 values (the NVFP4 scale layout), and the dequantizer multiplies the
+ * E2M1 value by 2^(b - 127) in bf16, exact for every scale byte b <= 252 (the
+ * weight itself overflows bf16 and FP32 above); accumulation in FP32. */
 qerl_status qerl_mxfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
                                        const uint8_t *codes, const uint8_t *scales, const void *A,
                                        const void *B, int r, float lora_scale, void *y, float *t_out,
                                        void *ws, size_t ws_bytes, qerl_stream_t stream);
 
 /* qerl_nvfp4_lora_linear_fwd (standard code layout) with FP32 LoRA adapters:
- * A (device) float [r, K], B (device) float [N, r]; t = x A^T and the LoRA
- * term are accumulated in FP32.  ws as for qerl_mxfp4_lora_linear_fwd. */
+ * A (device) float [r, K], B (device) float [N, r]; t = x A^T is accumulated
+ * in FP32.  The LoRA term: FP32 on the CUDA-core GEMM; on the tensor-core
+ * path, with u = s t / (s_t 2^c) split as u_hi = bf16(u), u_lo = bf16(u - u_hi)
+ * and B likewise, the three products B_hi u_hi + B_hi u_lo + B_lo u_hi
+ * accumulated in FP32 (relative error about 2^-16 of the term). */
 qerl_status qerl_nvfp4_lora_linear_fwd_f32ab(const void *x, int64_t M, int64_t K, int64_t N,
                                              const uint8_t *codes, const uint8_t *scales,
                                              const float *tensor_scale, const float *A, const float *B,

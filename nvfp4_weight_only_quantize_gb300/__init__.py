@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "QERL_OK", 1: "QERL_ERR_INVALID_ARG", 2: "QERL_ERR_SHAPE", 3:
                 7: "QERL_ERR_UNSUPPORTED_DEVICE", 8: "QERL_ERR_WORKSPACE", 9: "QERL_ERR_TOO_LARGE"}
 NOALLOC_SCRATCH_BYTES = 8 << 20  # QERL_NOALLOC_SCRATCH_BYTES
 SCALE_ROUND_UP, SCALE_ROUND_NEAREST_EVEN = 0, 1
-OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_AQN_RMSNORM = 0, 1, 2, 3
+OP_QUANTIZE, OP_LINEAR_FWD, OP_LINEAR_BWD, OP_AQN_RMSNORM, OP_MXFP4_FWD, OP_LINEAR_FWD_F32AB = 0, 1, 2, 3, 4, 5
 ALGO_AUTO, ALGO_SIMT, ALGO_TCGEN05, ALGO_GEMV = 0, 1, 2, 3
 AQN_NOISE_ADD, AQN_NOISE_MUL = 0, 1
 
@@ -315,20 +315,14 @@ def qerl_mxfp4_quantize(W: torch.Tensor, out=None, stream=None):
     return codes, scales
 
 
-def _t_ws(M, r, t_out, ws, device):
-    if t_out is None and ws is None:
-        ws = torch.empty(max(((M * r * 4 + 255) // 256) * 256, 1), dtype=torch.uint8, device=device)
-    return ws
-
-
 def qerl_mxfp4_lora_linear_fwd(x, codes, scales, A, B, lora_scale: float, y=None, t_out=None, ws=None, stream=None):
     M, K = x.shape
     N, r = B.shape
     y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
-    ws = _t_ws(M, r, t_out, ws, x.device)
+    ws = workspace(OP_MXFP4_FWD, M, N, K, r, x.device) if ws is None else ws
     _check(lib().qerl_mxfp4_lora_linear_fwd(_p(x), M, K, N, _p(codes), _p(scales), _p(A), _p(B), r, float(lora_scale),
-                                            _p(y), _p(t_out), _p(ws), 0 if ws is None else ws.numel(),
-                                            _stream(stream)), "qerl_mxfp4_lora_linear_fwd")
+                                            _p(y), _p(t_out), _p(ws), ws.numel(), _stream(stream)),
+           "qerl_mxfp4_lora_linear_fwd")
     return y
 
 
@@ -339,10 +333,10 @@ def qerl_nvfp4_lora_linear_fwd_f32ab(x, codes, scales, tensor_scale, A, B, lora_
     M, K = x.shape
     N, r = B.shape
     y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device) if y is None else y
-    ws = _t_ws(M, r, t_out, ws, x.device)
+    ws = workspace(OP_LINEAR_FWD_F32AB, M, N, K, r, x.device) if ws is None else ws
     _check(lib().qerl_nvfp4_lora_linear_fwd_f32ab(_p(x), M, K, N, _p(codes), _p(scales), _p(tensor_scale), _p(A),
-                                                  _p(B), r, float(lora_scale), _p(y), _p(t_out), _p(ws),
-                                                  0 if ws is None else ws.numel(), _stream(stream)),
+                                                  _p(B), r, float(lora_scale), _p(y), _p(t_out), _p(ws), ws.numel(),
+                                                  _stream(stream)),
            "qerl_nvfp4_lora_linear_fwd_f32ab")
     return y
 

@@ -99,6 +99,8 @@ extern "C" size_t qerl_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, 
     case QERL_OP_AQN_RMSNORM: return round256(size_t(K) * sizeof(float));  // K = H: noisy scale
     case QERL_OP_LINEAR_FWD: return linear_fwd_ws_bytes(M, N, K, r);
     case QERL_OP_LINEAR_BWD: return linear_bwd_ws_bytes(M, N, K, r);
+    case QERL_OP_MXFP4_FWD:
+    case QERL_OP_LINEAR_FWD_F32AB: return variant_fwd_ws_bytes(op, M, N, K, r);
     }
     return 0;
 }

@@ -49,4 +49,29 @@ __device__ __forceinline__ void dequant_word(uint32_t q, uint32_t f2, uint32_t *
     }
 }
 
+// MXFP4 block scale (OCP MX: E8M0 byte b, scale 2^(b - 127)): bf16x2 factors
+// fa, fb with fa * fb = 2^(b - 1), both normal bf16 for every b <= 254 (b = 255,
+// the NaN scale, gives fb = NaN).  b20 holds b in bits 20..27.  With the codes
+// placed as e2m1 * 2^-126 (dequant_word), (raw * fa) * fb = e2m1 * 2^(b - 127)
+// exactly: for b <= 128 the first product is already the value (on the bf16
+// subnormal grid at the smallest scales) and fb = 1; above, the first product
+// is e2m1 * 2 and fb = 2^(b - 128).
+__device__ __forceinline__ void mx_scale_factors(uint32_t b20, uint32_t &fa, uint32_t &fb)
+{
+    const uint32_t b = (b20 >> 20) & 0xFFu;
+    const uint32_t ea = (b < 128u ? b : 128u) + 126u;  // exponent field of 2^(min(b, 128) - 1)
+    const uint32_t eb = (b > 128u ? b : 128u) - 1u;    // exponent field of 2^(max(b, 128) - 128)
+    fa = (ea << 7) * 0x10001u;
+    fb = b == 255u ? 0x7FC07FC0u : (eb << 7) * 0x10001u;
+}
+
+// Eight E2M1 codes of an MXFP4 block -> four bf16x2 words e2m1 * 2^(b - 127).
+template <bool PACKED>
+__device__ __forceinline__ void dequant_word_mx(uint32_t q, uint32_t fa, uint32_t fb, uint32_t *out)
+{
+    dequant_word<PACKED>(q, fa, out);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[j] = ptx::bf16x2_mul(out[j], fb);
+}
+
 }  // namespace qerl

@@ -70,7 +70,8 @@ __device__ __forceinline__ float wprime_mx(const uint8_t *codes, const uint8_t *
     const uint32_t byte = codes[n * (K / 2) + k / 2];
     const uint32_t c = (k & 1) ? (byte >> 4) : (byte & 15u);
     const uint32_t b = scales[n * (K / 32) + k / 32];
-    const float sc = b != 0u ? __uint_as_float(b << 23) : __uint_as_float(1u << 22);  // 2^(b-127); b = 0: 2^-127
+    // 2^(b-127); b = 0: 2^-127; b = 255: NaN (the OCP NaN scale)
+    const float sc = b == 255u ? __uint_as_float(0x7FC00000u) : b != 0u ? __uint_as_float(b << 23) : __uint_as_float(1u << 22);
     return e2m1_to_float(c) * sc;
 }
 struct WRowMX {  // (n, k)
@@ -1144,41 +1145,63 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_grouped(const void *x, int64_t
 }
 
 namespace {
+// Scratch of a format-variant forward: what the tensor-core path needs where
+// it covers the shape, and at least t (FP32 [M, r]) for the CUDA-core GEMM.
+size_t variant_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool mx, bool f32)
+{
+    return std::max(tc_fwd_variant_ws_bytes(M, N, K, r, mx, f32), round256(size_t(M) * r * sizeof(float)));
+}
+
 qerl_status variant_args(const void *x, int64_t M, int64_t K, int64_t N, const uint8_t *codes, const uint8_t *scales,
-                         const void *A, const void *B, int r, void *y, float *t_out, void *ws, size_t ws_bytes,
-                         int kmul)
+                         const void *A, const void *B, int r, void *y, void *ws, size_t ws_bytes, int kmul, bool mx)
 {
     if (!codes || !scales || !A || !B) return QERL_ERR_INVALID_ARG;
     if (M < 0 || K < 1 || N < 1) return QERL_ERR_INVALID_ARG;
     if (K % kmul != 0 || r < 1 || r > 256) return QERL_ERR_SHAPE;
     if (M == 0) return QERL_OK;
     if (!x || !y) return QERL_ERR_INVALID_ARG;
-    if (!t_out && (!ws || ws_bytes < round256(size_t(M) * r * sizeof(float)))) return QERL_ERR_WORKSPACE;
+    if (!ws || ws_bytes < variant_ws_bytes(M, N, K, r, mx, !mx)) return QERL_ERR_WORKSPACE;
     return QERL_OK;
+}
+
+// The tensor-core path takes a variant unless the CUDA-core GEMM is selected or
+// an operand is not 16-byte aligned (its TMA maps and vector loads need that);
+// it declines shapes it does not cover (K % 256 != 0) with QERL_ERR_SHAPE.
+bool variant_tc_ok(const void *x, const void *y, const uint8_t *codes, const uint8_t *scales, const void *A,
+                   const void *B, const float *t_out)
+{
+    return g_algo.load() != QERL_ALGO_SIMT && aligned16(x) && aligned16(y) && aligned16(codes) &&
+           aligned16(scales) && aligned16(A) && aligned16(B) && (!t_out || aligned16(t_out));
 }
 }  // namespace
 
-// MXFP4 weight (codes [N, K/2], E8M0 scales [N, K/32]), bf16 LoRA; CUDA cores.
+// MXFP4 weight (codes [N, K/2], E8M0 scales [N, K/32]), bf16 LoRA: tcgen05 with
+// the E8M0 scale in the dequantizer, else the CUDA-core GEMM.
 extern "C" qerl_status qerl_mxfp4_lora_linear_fwd(const void *x, int64_t M, int64_t K, int64_t N,
                                                   const uint8_t *codes, const uint8_t *scales, const void *A,
                                                   const void *B, int r, float lora_scale, void *y, float *t_out,
                                                   void *ws, size_t ws_bytes, qerl_stream_t stream)
 {
-    QERL_TRY(variant_args(x, M, K, N, codes, scales, A, B, r, y, t_out, ws, ws_bytes, 32));
+    QERL_TRY(variant_args(x, M, K, N, codes, scales, A, B, r, y, ws, ws_bytes, 32, true));
     if (M == 0) return QERL_OK;
     QERL_TRY(check_device());
     cudaStream_t s = as_cuda(stream);
     const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    const __nv_bfloat16 *Ab = static_cast<const __nv_bfloat16 *>(A), *Bb = static_cast<const __nv_bfloat16 *>(B);
+    if (variant_tc_ok(x, y, codes, scales, A, B, t_out)) {
+        const FwdArgs a{xb, M, K, N, codes, nullptr, nullptr, Ab, Bb, r, lora_scale, static_cast<__nv_bfloat16 *>(y),
+                        t_out};
+        const qerl_status st = tc_fwd_variant(a, scales, static_cast<char *>(ws), ws_bytes, s);
+        if (st != QERL_ERR_SHAPE) return st;
+    }
     float *t = t_out ? t_out : static_cast<float *>(ws);
-    QERL_TRY(run_gemm(M, (int64_t)r, K, RowBF16{xb, K}, RowBF16{static_cast<const __nv_bfloat16 *>(A), K},
-                      StoreF32{t, r, 1.0f, 0}, s));
+    QERL_TRY(run_gemm(M, (int64_t)r, K, RowBF16{xb, K}, RowBF16{Ab, K}, StoreF32{t, r, 1.0f, 0}, s));
     return run_gemm(M, N, K, RowBF16{xb, K}, WRowMX{codes, scales, K},
-                    FwdEpiF32{static_cast<__nv_bfloat16 *>(y), N, nullptr, t, nullptr,
-                              static_cast<const __nv_bfloat16 *>(B), r, lora_scale},
-                    s);
+                    FwdEpiF32{static_cast<__nv_bfloat16 *>(y), N, nullptr, t, nullptr, Bb, r, lora_scale}, s);
 }
 
-// NVFP4 weight with FP32 LoRA adapters A [r, K], B [N, r]; CUDA cores.
+// NVFP4 weight with FP32 LoRA adapters A [r, K], B [N, r]: tcgen05 with the
+// LoRA term as three bf16 products of hi/lo splits, else the CUDA-core GEMM.
 extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_f32ab(const void *x, int64_t M, int64_t K, int64_t N,
                                                         const uint8_t *codes, const uint8_t *scales,
                                                         const float *tensor_scale, const float *A, const float *B,
@@ -1186,13 +1209,28 @@ extern "C" qerl_status qerl_nvfp4_lora_linear_fwd_f32ab(const void *x, int64_t M
                                                         size_t ws_bytes, qerl_stream_t stream)
 {
     if (!tensor_scale) return QERL_ERR_INVALID_ARG;
-    QERL_TRY(variant_args(x, M, K, N, codes, scales, A, B, r, y, t_out, ws, ws_bytes, 16));
+    QERL_TRY(variant_args(x, M, K, N, codes, scales, A, B, r, y, ws, ws_bytes, 16, false));
     if (M == 0) return QERL_OK;
     QERL_TRY(check_device());
     cudaStream_t s = as_cuda(stream);
     const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    if (variant_tc_ok(x, y, codes, scales, A, B, t_out)) {
+        FwdArgs a{xb, M, K, N, codes, scales, tensor_scale, nullptr, nullptr, r, lora_scale,
+                  static_cast<__nv_bfloat16 *>(y), t_out};
+        a.Af = A;
+        a.Bf = B;
+        const qerl_status st = tc_fwd_variant(a, nullptr, static_cast<char *>(ws), ws_bytes, s);
+        if (st != QERL_ERR_SHAPE) return st;
+    }
     float *t = t_out ? t_out : static_cast<float *>(ws);
     QERL_TRY(run_gemm(M, (int64_t)r, K, RowBF16{xb, K}, RowF32{A, K}, StoreF32{t, r, 1.0f, 0}, s));
     return run_gemm(M, N, K, RowBF16{xb, K}, WRow{codes, scales, K, 0},
                     FwdEpiF32{static_cast<__nv_bfloat16 *>(y), N, tensor_scale, t, B, nullptr, r, lora_scale}, s);
+}
+
+// Scratch of the format-variant forwards (QERL_OP_MXFP4_FWD, QERL_OP_LINEAR_FWD_F32AB).
+size_t qerl::variant_fwd_ws_bytes(int op, int64_t M, int64_t N, int64_t K, int r)
+{
+    if (op == QERL_OP_MXFP4_FWD) return K % 32 == 0 ? variant_ws_bytes(M, N, K, r, true, false) : 0;
+    return K % 16 == 0 ? variant_ws_bytes(M, N, K, r, false, true) : 0;
 }

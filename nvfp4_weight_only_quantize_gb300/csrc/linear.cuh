@@ -19,6 +19,13 @@ struct FwdArgs {
     __nv_bfloat16 *y;
     float *t_out;
     int packed = 0;  // codes in the packed layout (packed_layout.cuh)
+    // MXFP4 weight on the tensor-core path: `scales` then holds the E8M0 byte
+    // of each block of 32 twice ([N, K/16], tc_fwd_variant) and tensor_scale
+    // points to 2^-7, which makes the kernels' exponent offset 7 and their
+    // output scale 1 (the E8M0 factor carries the whole scale).
+    int mx = 0;
+    // FP32 LoRA adapters (A [r, K], B [N, r]) in place of A and B when set.
+    const float *Af = nullptr, *Bf = nullptr;
 };
 
 struct BwdArgs {
@@ -38,6 +45,8 @@ struct BwdArgs {
 
 size_t linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 size_t linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+// QERL_OP_MXFP4_FWD or QERL_OP_LINEAR_FWD_F32AB (qerl_workspace_bytes).
+size_t variant_fwd_ws_bytes(int op, int64_t M, int64_t N, int64_t K, int r);
 
 // Tensor-core (tcgen05) path.  Returns QERL_ERR_SHAPE, having launched nothing,
 // when it does not cover the call; the caller then runs the CUDA-core path.
@@ -46,6 +55,12 @@ qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStrea
 // G (<= 3) linears sharing x, M, K, r, lora_scale and layout in one launch.
 qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, cudaStream_t s);
 size_t tc_fwd_groups_ws_bytes(int64_t M, const int64_t *N, int G, int64_t K, int r);
+// Format variants on the tensor-core path (one linear): an MXFP4 weight
+// (mx_scales: E8M0 bytes [N, K/32], 16-byte aligned; a.codes in the standard
+// layout) and/or FP32 adapters (a.Af, a.Bf).  Scratch need, 0 when the path
+// does not cover the shape; QERL_ERR_SHAPE, having launched nothing, then.
+size_t tc_fwd_variant_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool mx, bool f32);
+qerl_status tc_fwd_variant(FwdArgs a, const uint8_t *mx_scales, char *ws, size_t ws_bytes, cudaStream_t s);
 // t = x A^T (FP32 [M, r] to `t`) and u = bf16(s t / (s_t 2^c)) ([M, r_pad],
 // zero past r; r_pad even) by the CUDA-core down-projection kernel, for
 // M <= 64 and K % 8 == 0.

@@ -121,6 +121,7 @@ struct TcGroups {
     const __nv_bfloat16 *Bl[MAX_GROUPS];
     const float *ts[MAX_GROUPS];
     __nv_bfloat16 *y[MAX_GROUPS];
+    const float *Bf[MAX_GROUPS];  // FP32 adapters: B as FP32 (lora_parts == 3)
 };
 // Tensor maps of a launch: per group codes, scales, LoRA A (fused) and u
 // (unfused); x is shared.
@@ -131,7 +132,8 @@ struct TcMaps {
 struct TcFwdParams {
     int M, K;
     int nk;              // K / BK main steps
-    int lora_steps;      // ceil(r / BK)
+    int lora_steps;      // lora_parts * ceil(r / BK)
+    int lora_parts;      // 1; 3 for FP32 adapters: B_hi u_hi + B_hi u_lo + B_lo u_hi
     int r, r_pad;        // rank, u row length (lora_steps * BK)
     int splits, steps_per_split;
     int n_tiles, m_tiles;  // weight tiles over all groups, token tiles
@@ -145,6 +147,26 @@ struct TcFwdParams {
 };
 
 
+// FP32 adapters: one weight row's A-operand values of a LoRA step, B_hi =
+// bf16(B) for parts 0 and 1, B_lo = bf16(B - B_hi) for part 2 (the token side
+// holds u_hi, u_lo, u_hi), columns jb .. jb + 63 (zero past r), stored to its
+// TMEM lane.  Out of line: inlined, its loads raise the register count of the
+// dequantizing loop it sits in.
+__device__ __noinline__ void lora_rows_f32(const float *brow, int jb, int r, bool row_ok, int part, uint32_t taddr)
+{
+    uint32_t out[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const int j = jb + 2 * e;
+        const float v0 = (row_ok && j < r) ? brow[j] : 0.0f;
+        const float v1 = (row_ok && j + 1 < r) ? brow[j + 1] : 0.0f;
+        __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+        if (part == 2) h = __floats2bfloat162_rn(v0 - __low2float(h), v1 - __high2float(h));
+        out[e] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    tmem_st32(taddr, out);
+}
+
 // 16 columns of this warp's 32 TMEM lanes of the accumulator, as floats.
 __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
 {
@@ -155,7 +177,7 @@ __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-template <int BN, bool PACKED, bool FUSED>
+template <int BN, bool PACKED, bool FUSED, bool MX = false>
 __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
     tc_fwd_kernel(const __grid_constant__ TcMaps maps, const TcFwdParams p)
 {
@@ -195,6 +217,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
     const int Ng = p.grp.N[g];
     const float *tsg = p.grp.ts[g];
     const __nv_bfloat16 *Blg = p.grp.Bl[g];
+    const float *Bfg = p.grp.Bf[g];
     __nv_bfloat16 *yg = p.grp.y[g];
     const CUtensorMap *codes_map = &maps.codes[g], *scl_map = &maps.scl[g], *al_map = &maps.al[g];
     const CUtensorMap *u_map = &maps.u[g], *x_map = &maps.x;
@@ -477,6 +500,20 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
             auto dequant_step = [&](int sub, uint32_t (&out)[32]) {
                 const uint4 c0 = cw[2 * sub], c1 = cw[2 * sub + 1];
                 const uint32_t sc = scw[sub];
+                if (MX) {  // bytes 0, 1 (and 2, 3) hold one 32-block's E8M0 byte twice
+                    uint32_t fa0, fb0, fa1, fb1;
+                    mx_scale_factors(sc << 20, fa0, fb0);
+                    mx_scale_factors(sc << 4, fa1, fb1);
+                    dequant_word_mx<PACKED>(c0.x, fa0, fb0, out + 0);
+                    dequant_word_mx<PACKED>(c0.y, fa0, fb0, out + 4);
+                    dequant_word_mx<PACKED>(c0.z, fa0, fb0, out + 8);
+                    dequant_word_mx<PACKED>(c0.w, fa0, fb0, out + 12);
+                    dequant_word_mx<PACKED>(c1.x, fa1, fb1, out + 16);
+                    dequant_word_mx<PACKED>(c1.y, fa1, fb1, out + 20);
+                    dequant_word_mx<PACKED>(c1.z, fa1, fb1, out + 24);
+                    dequant_word_mx<PACKED>(c1.w, fa1, fb1, out + 28);
+                    return;
+                }
                 const uint32_t f0 = scale_factor_bf16x2(sc << 20, pow2);
                 const uint32_t f1 = scale_factor_bf16x2(sc << 12, pow2);
                 const uint32_t f2 = scale_factor_bf16x2(sc << 4, pow2);
@@ -514,6 +551,12 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                     // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
                     // (Chained: B may be written by work before this call.)
                     if (p.chain) pdl_wait();
+                    if (p.lora_parts == 3) {  // FP32 adapters: B_hi or B_lo, stored out of line
+                        const int L = p.lora_steps / 3, q = i - n_main, part = q / L;
+                        lora_rows_f32(Bfg + (size_t)(row_ok ? n : 0) * p.r, (q - part * L) * BK, p.r, row_ok, part,
+                                      taddr);
+                        continue;
+                    }
                     const int j0 = (i - n_main) * BK;
                     const __nv_bfloat16 *b = Blg + (size_t)(row_ok ? n : 0) * p.r + j0;
                     if (row_ok && (p.r & 7) == 0 && j0 + 64 <= p.r) {
@@ -617,14 +660,18 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
 // MB token rows x JB adapter rows; its 256 threads stride over K in 8-element
 // vectors and the partial sums are reduced in shared memory in a fixed order.
 // The main kernel may start (programmatic launch) while this kernel runs.
+// AF32 (FP32 adapters): A is FP32 and each u row is [u_hi | u_lo | u_hi]
+// (3 r_pad values, u_lo = bf16(t s / ysc - u_hi)) for the three LoRA products.
 constexpr int LD_THREADS = 256;
 
-template <int MB, int JB>
+template <int MB, int JB, bool AF32 = false>
 __global__ void __launch_bounds__(LD_THREADS)
-    lora_down_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ A, int M, int K, int r,
+    lora_down_kernel(const __nv_bfloat16 *__restrict__ x, const void *__restrict__ Av, int M, int K, int r,
                      int r_pad, float s, const float *__restrict__ tensor_scale, float *__restrict__ t_out,
                      __nv_bfloat16 *__restrict__ u)
 {
+    const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(Av);
+    const float *Af = static_cast<const float *>(Av);
     __shared__ float red[LD_THREADS / 32][MB * JB];
     pdl_trigger();  // the main kernel may start streaming its weight now
     pdl_wait();     // chained launch: x and A follow the preceding work
@@ -639,11 +686,26 @@ __global__ void __launch_bounds__(LD_THREADS)
     if (j0 < r) {
 #pragma unroll 2
         for (int k = threadIdx.x * 8; k < K; k += LD_THREADS * 8) {
-            uint4 av[JB], xv[MB];
+            float af[JB][8];  // A[j0 + b, k .. k + 7]
 #pragma unroll
-            for (int b = 0; b < JB; ++b)
-                av[b] = (j0 + b < r) ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)(j0 + b) * K + k))
-                                     : make_uint4(0u, 0u, 0u, 0u);
+            for (int b = 0; b < JB; ++b) {
+                if (AF32) {
+                    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+                    if (j0 + b < r) {
+                        lo = __ldg(reinterpret_cast<const float4 *>(Af + (size_t)(j0 + b) * K + k));
+                        hi = __ldg(reinterpret_cast<const float4 *>(Af + (size_t)(j0 + b) * K + k) + 1);
+                    }
+                    af[b][0] = lo.x, af[b][1] = lo.y, af[b][2] = lo.z, af[b][3] = lo.w;
+                    af[b][4] = hi.x, af[b][5] = hi.y, af[b][6] = hi.z, af[b][7] = hi.w;
+                } else {
+                    const uint4 v = (j0 + b < r) ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)(j0 + b) * K + k))
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t aw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) af[b][2 * q] = bf16lo(aw[q]), af[b][2 * q + 1] = bf16hi(aw[q]);
+                }
+            }
+            uint4 xv[MB];
 #pragma unroll
             for (int a = 0; a < MB; ++a)
                 xv[a] = (m0 + a < M) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + a) * K + k))
@@ -653,12 +715,11 @@ __global__ void __launch_bounds__(LD_THREADS)
                 const uint32_t xw[4] = {xv[a].x, xv[a].y, xv[a].z, xv[a].w};
 #pragma unroll
                 for (int b = 0; b < JB; ++b) {
-                    const uint32_t aw[4] = {av[b].x, av[b].y, av[b].z, av[b].w};
                     float t = acc[a][b];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        t = fmaf(bf16lo(xw[q]), bf16lo(aw[q]), t);
-                        t = fmaf(bf16hi(xw[q]), bf16hi(aw[q]), t);
+                        t = fmaf(bf16lo(xw[q]), af[b][2 * q], t);
+                        t = fmaf(bf16hi(xw[q]), af[b][2 * q + 1], t);
                     }
                     acc[a][b] = t;
                 }
@@ -682,13 +743,19 @@ __global__ void __launch_bounds__(LD_THREADS)
             float t = 0.0f;
 #pragma unroll
             for (int w = 0; w < LD_THREADS / 32; ++w) t += red[w][threadIdx.x];
+            const int ld = AF32 ? 3 * r_pad : r_pad;
+            __nv_bfloat16 uh = __float2bfloat16_rn(0.0f), ul = uh;
             if (j < r) {
                 const float st = *tensor_scale;
                 const float fac = s / (st * pow2f(tc_exponent_offset(st)));
                 if (t_out) t_out[(size_t)m * r + j] = t;
-                u[(size_t)m * r_pad + j] = __float2bfloat16_rn(t * fac);
-            } else {
-                u[(size_t)m * r_pad + j] = __float2bfloat16_rn(0.0f);
+                uh = __float2bfloat16_rn(t * fac);
+                ul = __float2bfloat16_rn(t * fac - __bfloat162float(uh));
+            }
+            u[(size_t)m * ld + j] = uh;
+            if (AF32) {
+                u[(size_t)m * ld + r_pad + j] = ul;
+                u[(size_t)m * ld + 2 * r_pad + j] = uh;
             }
         }
     }
@@ -757,8 +824,9 @@ struct FwdPlan {
 
 // Launch plan for G linears sharing x: their weight tiles side by side, one
 // split factor, one u region per group, the split partials, and (one linear,
-// many tokens) the partials of the rows x rank down-projection.
-FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r)
+// many tokens) the partials of the rows x rank down-projection.  parts = 3
+// (FP32 adapters): three LoRA products, u rows of 3 r_pad values.
+FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r, int parts = 1)
 {
     FwdPlan pl;
     pl.BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
@@ -766,8 +834,8 @@ FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r)
     for (int g = 0; g < G; ++g) pl.n_tiles += (int)((N[g] + TILE_N - 1) / TILE_N);
     pl.m_tiles = (int)((M + pl.BN - 1) / pl.BN);
     pl.nk = (int)(K / BK);
-    pl.lora_steps = (r + BK - 1) / BK;
-    pl.r_pad = pl.lora_steps * BK;
+    pl.lora_steps = parts * ((r + BK - 1) / BK);
+    pl.r_pad = (r + BK - 1) / BK * BK;
     const int64_t tiles = (int64_t)pl.n_tiles * pl.m_tiles;
     const int sms = num_sms();
     int splits = 1;
@@ -781,13 +849,14 @@ FwdPlan plan_fwd(int64_t M, const int64_t *N, int G, int64_t K, int r)
     pl.sps = (pl.nk + splits - 1) / splits;
     pl.sps = (pl.sps + GK - 1) / GK * GK;  // splits start on a raw-stage boundary
     pl.splits = (pl.nk + pl.sps - 1) / pl.sps;  // no empty split
-    pl.u_bytes = round256(size_t(M) * pl.r_pad * 2);
+    pl.u_bytes = round256(size_t(M) * pl.r_pad * parts * 2);
     pl.off_u = 0;
     pl.off_part = pl.u_bytes * G;
     pl.off_rows = pl.off_part + (pl.splits > 1 ? size_t(tiles) * pl.splits * TILE_N * pl.BN * 4 : 0);
     // many tokens: the down-projection runs as a split-K rows x rank product
     // (one pass over x for every group)
-    pl.total = pl.off_rows + (M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r, G) : 0);
+    pl.total = pl.off_rows +
+               (parts == 1 && M > 64 && lora_down_rows_applies(K, r) ? lora_down_rows_ws(M, K, r, G) : 0);
     return pl;
 }
 
@@ -820,10 +889,15 @@ const Env &env()
 }
 
 template <int BN, bool FUSED>
-qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid, bool packed, bool pdl, cudaStream_t s)
+qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid, bool packed, bool mx, bool pdl,
+                       cudaStream_t s)
 {
     using C = Cfg<BN, FUSED>;
     auto kernel = packed ? tc_fwd_kernel<BN, true, FUSED> : tc_fwd_kernel<BN, false, FUSED>;
+    if constexpr (!FUSED) {  // MXFP4 weights: standard code layout, separate down-projection
+        if (mx) kernel = tc_fwd_kernel<BN, false, false, true>;
+    }
+    if (mx && (FUSED || packed)) return QERL_ERR_SHAPE;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return QERL_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -904,6 +978,10 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
 {
     if (G < 1 || G > MAX_GROUPS) return QERL_ERR_SHAPE;
     const FwdArgs &a = ga[0];
+    // format variants (one linear): MXFP4 weights, FP32 adapters
+    const bool mx = a.mx != 0, f32 = a.Af != nullptr;
+    const int parts = f32 ? 3 : 1;
+    if ((mx || f32) && (G != 1 || (mx && a.packed) || (f32 && !a.Bf))) return QERL_ERR_SHAPE;
     int64_t Ns[MAX_GROUPS];
     bool any_t = false;
     for (int g = 0; g < G; ++g) {
@@ -911,7 +989,7 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
         Ns[g] = ga[g].N;
         any_t = any_t || ga[g].t_out;
     }
-    const FwdPlan pl = plan_fwd(a.M, Ns, G, a.K, a.r);
+    const FwdPlan pl = plan_fwd(a.M, Ns, G, a.K, a.r, parts);
     if (ws_bytes < pl.total) return QERL_ERR_WORKSPACE;
     float *partial = reinterpret_cast<float *>(ws + pl.off_part);
     const int tiles = pl.n_tiles * pl.m_tiles;
@@ -920,8 +998,9 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     // not requested, for split launches and for groups.  A single unsplit
     // linear keeps the separate grid: it overlaps the long weight stream, while
     // the fused MMAs would load it.
-    const bool fused = !any_t && pl.BN <= 64 && a.r <= FUSED_R && (pl.splits > 1 || G > 1) && !env().no_fuse;
-    TcMaps maps;
+    const bool fused = !any_t && !mx && !f32 && pl.BN <= 64 && a.r <= FUSED_R && (pl.splits > 1 || G > 1) &&
+                       !env().no_fuse;
+    TcMaps maps = {};
     // codes: 128 rows x 128 bytes (4 k-steps) per box, 128-byte swizzle; scales:
     // 128 rows x 16 bytes (the same 4 k-steps); token tiles: BN rows x 64 bf16;
     // fused: LoRA A rows 0..31 x 64 bf16 (zero past r).
@@ -935,10 +1014,10 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
                          TILE_N, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map_2d(&maps.scl[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, b.scales, a.K / 16, b.N, a.K / 16,
                          GK * BK / 16, TILE_N, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !make_map_2d(&maps.u[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, pl.r_pad, a.M, pl.r_pad * 2, BK, pl.BN,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_map_2d(&maps.al[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.A, a.K, a.r, a.K * 2, BK, FUSED_R,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+            !make_map_2d(&maps.u[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, u, pl.r_pad * parts, a.M,
+                         pl.r_pad * parts * 2, BK, pl.BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            (fused && !make_map_2d(&maps.al[g], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b.A, a.K, a.r, a.K * 2, BK, FUSED_R,
+                                   CU_TENSOR_MAP_SWIZZLE_128B)))
             return QERL_ERR_CUDA;
     }
 
@@ -947,7 +1026,7 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     //    the main kernel may then stream and dequantize its (frozen) weight
     //    while that work is still running.
     const bool chain = g_chain.load() != 0;
-    const bool rows = !fused && a.M > 64 && lora_down_rows_applies(a.K, a.r);
+    const bool rows = !fused && !f32 && a.M > 64 && lora_down_rows_applies(a.K, a.r);
     if (rows) {
         DownRowsGroup dg[MAX_GROUPS];
         for (int g = 0; g < G; ++g)
@@ -959,18 +1038,19 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     for (int g = 0; g < G && !fused && !rows; ++g) {
         const FwdArgs &b = ga[g];
         __nv_bfloat16 *u = reinterpret_cast<__nv_bfloat16 *>(ws + pl.off_u + g * pl.u_bytes);
+        const void *Av = f32 ? static_cast<const void *>(b.Af) : static_cast<const void *>(b.A);
         if (a.M <= 64) {  // few registers: its CTAs can share SMs with the main kernel's
             constexpr int MB = 4, JB = 2;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
-            QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
-                                       b.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, b.tensor_scale,
-                                       b.t_out, u)));
+            auto k = f32 ? lora_down_kernel<MB, JB, true> : lora_down_kernel<MB, JB, false>;
+            QERL_TRY(launched(launch_k(k, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x, Av, (int)a.M, (int)a.K,
+                                       a.r, pl.r_pad, a.lora_scale, b.tensor_scale, b.t_out, u)));
         } else {
             constexpr int MB = 8, JB = 4;
             const unsigned blocks = (unsigned)(((a.M + MB - 1) / MB) * (pl.r_pad / JB));
-            QERL_TRY(launched(launch_k(lora_down_kernel<MB, JB>, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x,
-                                       b.A, (int)a.M, (int)a.K, a.r, pl.r_pad, a.lora_scale, b.tensor_scale,
-                                       b.t_out, u)));
+            auto k = f32 ? lora_down_kernel<MB, JB, true> : lora_down_kernel<MB, JB, false>;
+            QERL_TRY(launched(launch_k(k, dim3(blocks), dim3(LD_THREADS), 0, s, chain, a.x, Av, (int)a.M, (int)a.K,
+                                       a.r, pl.r_pad, a.lora_scale, b.tensor_scale, b.t_out, u)));
         }
     }
 
@@ -980,6 +1060,7 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     p.K = (int)a.K;
     p.nk = pl.nk;
     p.lora_steps = pl.lora_steps;
+    p.lora_parts = parts;
     p.r = a.r;
     p.r_pad = pl.r_pad;
     p.splits = pl.splits;
@@ -996,6 +1077,7 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
         p.grp.Bl[g] = b.B;
         p.grp.ts[g] = b.tensor_scale;
         p.grp.y[g] = b.y;
+        p.grp.Bf[g] = b.Bf;
     }
     p.grp.tile_start[MAX_GROUPS] = t0;
     p.partial = partial;
@@ -1011,16 +1093,19 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     const bool pk = a.packed != 0, pdl = fused ? chain : true;
     switch (pl.BN) {
     case 16:
-        st = fused ? launch_fwd<16, true>(maps, p, grid, pk, pdl, s) : launch_fwd<16, false>(maps, p, grid, pk, pdl, s);
+        st = fused ? launch_fwd<16, true>(maps, p, grid, pk, mx, pdl, s)
+                   : launch_fwd<16, false>(maps, p, grid, pk, mx, pdl, s);
         break;
     case 32:
-        st = fused ? launch_fwd<32, true>(maps, p, grid, pk, pdl, s) : launch_fwd<32, false>(maps, p, grid, pk, pdl, s);
+        st = fused ? launch_fwd<32, true>(maps, p, grid, pk, mx, pdl, s)
+                   : launch_fwd<32, false>(maps, p, grid, pk, mx, pdl, s);
         break;
     case 64:
-        st = fused ? launch_fwd<64, true>(maps, p, grid, pk, pdl, s) : launch_fwd<64, false>(maps, p, grid, pk, pdl, s);
+        st = fused ? launch_fwd<64, true>(maps, p, grid, pk, mx, pdl, s)
+                   : launch_fwd<64, false>(maps, p, grid, pk, mx, pdl, s);
         break;
-    case 128: st = launch_fwd<128, false>(maps, p, grid, pk, pdl, s); break;
-    default: st = launch_fwd<256, false>(maps, p, grid, pk, pdl, s); break;
+    case 128: st = launch_fwd<128, false>(maps, p, grid, pk, mx, pdl, s); break;
+    default: st = launch_fwd<256, false>(maps, p, grid, pk, mx, pdl, s); break;
     }
     if (st != QERL_OK || pl.splits == 1) return st;
     // 3) split-K: sum the partial tiles (chained: waits for the main grid)
@@ -1050,6 +1135,60 @@ qerl_status lora_down_small(const FwdArgs &a, int r_pad, float *t, __nv_bfloat16
 
 qerl_status tc_linear_fwd(const FwdArgs &a, char *ws, size_t ws_bytes, cudaStream_t s)
 {
+    return tc_fwd_groups(&a, 1, ws, ws_bytes, s);
+}
+
+namespace {
+// MXFP4 scales for the tensor-core path: each E8M0 byte of [N, K/32] written
+// twice into [N, K/16] (the per-16 scale layout the raw stages load), and the
+// tensor scale 2^-7 (exponent offset 7, output scale 1).  It never triggers
+// its dependents early, so the kernels after it may read both before their
+// own programmatic wait; it waits for the preceding work before writing (that
+// work may still read the workspace).
+__global__ void __launch_bounds__(256) mx_expand_scales_kernel(const uint8_t *__restrict__ s32, int64_t n8,
+                                                               uint8_t *__restrict__ s16, float *__restrict__ ts)
+{
+    pdl_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ts = 0.0078125f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(s32) + i);  // 8 bytes -> 16
+        uint4 o;
+        o.x = prmt(v.x, 0u, 0x1100u);
+        o.y = prmt(v.x, 0u, 0x3322u);
+        o.z = prmt(v.y, 0u, 0x1100u);
+        o.w = prmt(v.y, 0u, 0x3322u);
+        reinterpret_cast<uint4 *>(s16)[i] = o;
+    }
+}
+}  // namespace
+
+size_t tc_fwd_variant_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool mx, bool f32)
+{
+    if (!tc_fwd_applies(M, N, K, r)) return 0;
+    const size_t lin = plan_fwd(M, &N, 1, K, r, f32 ? 3 : 1).total;
+    return mx ? round256(size_t(N) * (K / 16)) + 256 + lin : lin;
+}
+
+qerl_status tc_fwd_variant(FwdArgs a, const uint8_t *mx_scales, char *ws, size_t ws_bytes, cudaStream_t s)
+{
+    const bool mx = mx_scales != nullptr;
+    if (!tc_fwd_applies(a.M, a.N, a.K, a.r) || (mx && a.packed)) return QERL_ERR_SHAPE;
+    if (ws_bytes < tc_fwd_variant_ws_bytes(a.M, a.N, a.K, a.r, mx, a.Af != nullptr)) return QERL_ERR_WORKSPACE;
+    if (mx) {
+        const size_t sb = round256(size_t(a.N) * (a.K / 16));
+        uint8_t *s16 = reinterpret_cast<uint8_t *>(ws);
+        float *ts = reinterpret_cast<float *>(ws + sb);
+        const int64_t n8 = a.N * (a.K / 256);  // K % 256 == 0: whole 8-byte groups
+        int64_t gr = (n8 + 255) / 256;
+        if (gr > 4 * num_sms()) gr = 4 * num_sms();
+        QERL_TRY(launched(launch_k(mx_expand_scales_kernel, dim3((unsigned)gr), dim3(256), 0, s, g_chain.load() != 0,
+                                   mx_scales, n8, s16, ts)));
+        a.scales = s16;
+        a.tensor_scale = ts;
+        a.mx = 1;
+        ws += sb + 256;
+        ws_bytes -= sb + 256;
+    }
     return tc_fwd_groups(&a, 1, ws, ws_bytes, s);
 }
 

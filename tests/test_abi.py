@@ -66,6 +66,17 @@ def test_argument_errors_return_before_any_launch(L):
     assert L.qerl_aqn_noise(0, 0, 0, 0, fake, None, None) == 1
     assert L.qerl_set_linear_algo(9) == 1
     assert L.qerl_set_linear_algo(4) == 1
+    # format variants: K % 32 (MXFP4) / K % 16, r, missing or short workspace
+    vargs = lambda K, r, wsp, wsb: (fake, 8, K, 16, fake, fake, fake, fake, r, 2.0, fake, None, wsp, wsb, None)
+    assert L.qerl_mxfp4_lora_linear_fwd(*vargs(48, 4, ws, 1 << 20)) == 2
+    assert L.qerl_mxfp4_lora_linear_fwd(*vargs(64, 0, ws, 1 << 20)) == 2
+    assert L.qerl_mxfp4_lora_linear_fwd(*vargs(64, 4, None, 0)) == 8
+    need = q.workspace_bytes(q.OP_MXFP4_FWD, 8, 16, 256, 4)
+    assert L.qerl_mxfp4_lora_linear_fwd(*vargs(256, 4, ws, need - 1)) == 8
+    fargs = lambda K, r, wsb: (fake, 8, K, 16, fake, fake, fake, fake, fake, r, 2.0, fake, None, ws, wsb, None)
+    assert L.qerl_nvfp4_lora_linear_fwd_f32ab(*fargs(40, 4, 1 << 20)) == 2
+    need = q.workspace_bytes(q.OP_LINEAR_FWD_F32AB, 8, 16, 256, 4)
+    assert L.qerl_nvfp4_lora_linear_fwd_f32ab(*fargs(256, 4, need - 1)) == 8
 
 
 def test_grouped_argument_errors_return_before_any_launch(L):
@@ -98,6 +109,15 @@ def test_workspace_covers_every_region(L):
     # backward: v and t (FP32), v' (bf16 [M, 64]), B^T (bf16 [r, N]), hi/lo pair (bf16 [M, 64]), partials
     M, N, K = 8192, 3584, 3584
     assert q.workspace_bytes(q.OP_LINEAR_BWD, M, N, K, r) >= 2 * M * r * 4 + M * 64 * 2 + r * N * 2 + M * 64 * 2
+    # format variants on tensor cores: MXFP4 keeps one scale byte per 16 values (and the 2^-7 tensor scale)
+    # beside u (bf16 [M, 64]); FP32 adapters keep u_hi | u_lo | u_hi (bf16 [M, 3 * 64]); the CUDA-core
+    # GEMM (K % 256 != 0) keeps t (FP32 [M, r])
+    M, N, K = 8, 18944, 3584
+    assert q.workspace_bytes(q.OP_MXFP4_FWD, M, N, K, r) >= N * K // 16 + 4 + M * 64 * 2
+    assert q.workspace_bytes(q.OP_LINEAR_FWD_F32AB, M, N, K, r) >= M * 3 * 64 * 2
+    assert q.workspace_bytes(q.OP_MXFP4_FWD, M, N, 96, r) >= M * r * 4
+    assert q.workspace_bytes(q.OP_LINEAR_FWD_F32AB, M, N, 48, r) >= M * r * 4
+    assert q.workspace_bytes(q.OP_MXFP4_FWD, M, N, 48, r) == 0  # K % 32 != 0: no MXFP4 call
 
 
 def test_sigma_schedule_matches_oracle(L):
