@@ -35,8 +35,8 @@ L2_BYTES = 129 * 1024 * 1024
 # of the decode step (the tc_fwd capture summarised under profiles/) of
 # csrc/linear_tc.cu with this sha256 prefix; reported as roofline.traffic only
 # while the source still matches.
-NCU_KERNEL_SHA = "87c1b361a89176dd"
-NCU_DRAM_BYTES = {"gate_proj": 39.934208e6, "up_proj": 39.933952e6, "down_proj": 42.137344e6}
+NCU_KERNEL_SHA = "d2196cbf4bdd07bb"
+NCU_DRAM_BYTES = {"gate_proj": 39.934208e6, "up_proj": 39.936512e6, "down_proj": 42.134272e6}
 
 
 def ncu_traffic(name):

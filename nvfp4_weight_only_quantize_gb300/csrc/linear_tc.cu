@@ -177,7 +177,9 @@ __device__ __forceinline__ void acc_load16(uint32_t taddr, float (&v)[16])
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-template <int BN, bool PACKED, bool FUSED, bool MX = false>
+// MX: MXFP4 weights (the E8M0 factor in the dequantizer).  F32AB: FP32
+// adapters (B converted to B_hi / B_lo for the three LoRA products).
+template <int BN, bool PACKED, bool FUSED, bool MX = false, bool F32AB = false>
 __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
     tc_fwd_kernel(const __grid_constant__ TcMaps maps, const TcFwdParams p)
 {
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED>::NUM_THREADS, 1)
                     // LoRA up-projection rows: B[n, l*64 .. +63], zero past r.
                     // (Chained: B may be written by work before this call.)
                     if (p.chain) pdl_wait();
-                    if (p.lora_parts == 3) {  // FP32 adapters: B_hi or B_lo, stored out of line
+                    if (F32AB) {  // FP32 adapters: B_hi or B_lo, stored out of line
                         const int L = p.lora_steps / 3, q = i - n_main, part = q / L;
                         lora_rows_f32(Bfg + (size_t)(row_ok ? n : 0) * p.r, (q - part * L) * BK, p.r, row_ok, part,
                                       taddr);
@@ -686,10 +688,18 @@ __global__ void __launch_bounds__(LD_THREADS)
     if (j0 < r) {
 #pragma unroll 2
         for (int k = threadIdx.x * 8; k < K; k += LD_THREADS * 8) {
-            float af[JB][8];  // A[j0 + b, k .. k + 7]
+            uint4 xv[MB];
+            auto load_x = [&] {
 #pragma unroll
-            for (int b = 0; b < JB; ++b) {
-                if (AF32) {
+                for (int a = 0; a < MB; ++a)
+                    xv[a] = (m0 + a < M) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + a) * K + k))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+            };
+            if constexpr (AF32) {
+                load_x();
+                float af[JB][8];  // A[j0 + b, k .. k + 7]
+#pragma unroll
+                for (int b = 0; b < JB; ++b) {
                     float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
                     if (j0 + b < r) {
                         lo = __ldg(reinterpret_cast<const float4 *>(Af + (size_t)(j0 + b) * K + k));
@@ -697,31 +707,42 @@ __global__ void __launch_bounds__(LD_THREADS)
                     }
                     af[b][0] = lo.x, af[b][1] = lo.y, af[b][2] = lo.z, af[b][3] = lo.w;
                     af[b][4] = hi.x, af[b][5] = hi.y, af[b][6] = hi.z, af[b][7] = hi.w;
-                } else {
-                    const uint4 v = (j0 + b < r) ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)(j0 + b) * K + k))
-                                                 : make_uint4(0u, 0u, 0u, 0u);
-                    const uint32_t aw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) af[b][2 * q] = bf16lo(aw[q]), af[b][2 * q + 1] = bf16hi(aw[q]);
                 }
-            }
-            uint4 xv[MB];
 #pragma unroll
-            for (int a = 0; a < MB; ++a)
-                xv[a] = (m0 + a < M) ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(m0 + a) * K + k))
-                                     : make_uint4(0u, 0u, 0u, 0u);
+                for (int a = 0; a < MB; ++a) {
+                    const uint32_t xw[4] = {xv[a].x, xv[a].y, xv[a].z, xv[a].w};
 #pragma unroll
-            for (int a = 0; a < MB; ++a) {
-                const uint32_t xw[4] = {xv[a].x, xv[a].y, xv[a].z, xv[a].w};
+                    for (int b = 0; b < JB; ++b) {
+                        float t = acc[a][b];
 #pragma unroll
-                for (int b = 0; b < JB; ++b) {
-                    float t = acc[a][b];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        t = fmaf(bf16lo(xw[q]), af[b][2 * q], t);
-                        t = fmaf(bf16hi(xw[q]), af[b][2 * q + 1], t);
+                        for (int q = 0; q < 4; ++q) {
+                            t = fmaf(bf16lo(xw[q]), af[b][2 * q], t);
+                            t = fmaf(bf16hi(xw[q]), af[b][2 * q + 1], t);
+                        }
+                        acc[a][b] = t;
                     }
-                    acc[a][b] = t;
+                }
+            } else {
+                uint4 av[JB];
+#pragma unroll
+                for (int b = 0; b < JB; ++b)
+                    av[b] = (j0 + b < r) ? __ldg(reinterpret_cast<const uint4 *>(A + (size_t)(j0 + b) * K + k))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                load_x();
+#pragma unroll
+                for (int a = 0; a < MB; ++a) {
+                    const uint32_t xw[4] = {xv[a].x, xv[a].y, xv[a].z, xv[a].w};
+#pragma unroll
+                    for (int b = 0; b < JB; ++b) {
+                        const uint32_t aw[4] = {av[b].x, av[b].y, av[b].z, av[b].w};
+                        float t = acc[a][b];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            t = fmaf(bf16lo(xw[q]), bf16lo(aw[q]), t);
+                            t = fmaf(bf16hi(xw[q]), bf16hi(aw[q]), t);
+                        }
+                        acc[a][b] = t;
+                    }
                 }
             }
         }
@@ -743,19 +764,26 @@ __global__ void __launch_bounds__(LD_THREADS)
             float t = 0.0f;
 #pragma unroll
             for (int w = 0; w < LD_THREADS / 32; ++w) t += red[w][threadIdx.x];
-            const int ld = AF32 ? 3 * r_pad : r_pad;
-            __nv_bfloat16 uh = __float2bfloat16_rn(0.0f), ul = uh;
-            if (j < r) {
+            if constexpr (AF32) {  // row [u_hi | u_lo | u_hi]
+                __nv_bfloat16 uh = __float2bfloat16_rn(0.0f), ul = uh;
+                if (j < r) {
+                    const float st = *tensor_scale;
+                    const float fac = s / (st * pow2f(tc_exponent_offset(st)));
+                    if (t_out) t_out[(size_t)m * r + j] = t;
+                    uh = __float2bfloat16_rn(t * fac);
+                    ul = __float2bfloat16_rn(t * fac - __bfloat162float(uh));
+                }
+                __nv_bfloat16 *row = u + (size_t)m * 3 * r_pad;
+                row[j] = uh;
+                row[r_pad + j] = ul;
+                row[2 * r_pad + j] = uh;
+            } else if (j < r) {
                 const float st = *tensor_scale;
                 const float fac = s / (st * pow2f(tc_exponent_offset(st)));
                 if (t_out) t_out[(size_t)m * r + j] = t;
-                uh = __float2bfloat16_rn(t * fac);
-                ul = __float2bfloat16_rn(t * fac - __bfloat162float(uh));
-            }
-            u[(size_t)m * ld + j] = uh;
-            if (AF32) {
-                u[(size_t)m * ld + r_pad + j] = ul;
-                u[(size_t)m * ld + 2 * r_pad + j] = uh;
+                u[(size_t)m * r_pad + j] = __float2bfloat16_rn(t * fac);
+            } else {
+                u[(size_t)m * r_pad + j] = __float2bfloat16_rn(0.0f);
             }
         }
     }
@@ -889,15 +917,17 @@ const Env &env()
 }
 
 template <int BN, bool FUSED>
-qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid, bool packed, bool mx, bool pdl,
-                       cudaStream_t s)
+qerl_status launch_fwd(const TcMaps &maps, const TcFwdParams &p0, unsigned grid, bool packed, bool mx, bool f32,
+                       bool pdl, cudaStream_t s)
 {
     using C = Cfg<BN, FUSED>;
     auto kernel = packed ? tc_fwd_kernel<BN, true, FUSED> : tc_fwd_kernel<BN, false, FUSED>;
-    if constexpr (!FUSED) {  // MXFP4 weights: standard code layout, separate down-projection
-        if (mx) kernel = tc_fwd_kernel<BN, false, false, true>;
+    // format variants: standard code layout, separate down-projection
+    if ((mx || f32) && (FUSED || packed)) return QERL_ERR_SHAPE;
+    if constexpr (!FUSED) {
+        if (mx) kernel = tc_fwd_kernel<BN, false, false, true, false>;
+        if (f32) kernel = tc_fwd_kernel<BN, false, false, false, true>;
     }
-    if (mx && (FUSED || packed)) return QERL_ERR_SHAPE;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return QERL_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1093,19 +1123,19 @@ qerl_status tc_fwd_groups(const FwdArgs *ga, int G, char *ws, size_t ws_bytes, c
     const bool pk = a.packed != 0, pdl = fused ? chain : true;
     switch (pl.BN) {
     case 16:
-        st = fused ? launch_fwd<16, true>(maps, p, grid, pk, mx, pdl, s)
-                   : launch_fwd<16, false>(maps, p, grid, pk, mx, pdl, s);
+        st = fused ? launch_fwd<16, true>(maps, p, grid, pk, mx, f32, pdl, s)
+                   : launch_fwd<16, false>(maps, p, grid, pk, mx, f32, pdl, s);
         break;
     case 32:
-        st = fused ? launch_fwd<32, true>(maps, p, grid, pk, mx, pdl, s)
-                   : launch_fwd<32, false>(maps, p, grid, pk, mx, pdl, s);
+        st = fused ? launch_fwd<32, true>(maps, p, grid, pk, mx, f32, pdl, s)
+                   : launch_fwd<32, false>(maps, p, grid, pk, mx, f32, pdl, s);
         break;
     case 64:
-        st = fused ? launch_fwd<64, true>(maps, p, grid, pk, mx, pdl, s)
-                   : launch_fwd<64, false>(maps, p, grid, pk, mx, pdl, s);
+        st = fused ? launch_fwd<64, true>(maps, p, grid, pk, mx, f32, pdl, s)
+                   : launch_fwd<64, false>(maps, p, grid, pk, mx, f32, pdl, s);
         break;
-    case 128: st = launch_fwd<128, false>(maps, p, grid, pk, mx, pdl, s); break;
-    default: st = launch_fwd<256, false>(maps, p, grid, pk, mx, pdl, s); break;
+    case 128: st = launch_fwd<128, false>(maps, p, grid, pk, mx, f32, pdl, s); break;
+    default: st = launch_fwd<256, false>(maps, p, grid, pk, mx, f32, pdl, s); break;
     }
     if (st != QERL_OK || pl.splits == 1) return st;
     // 3) split-K: sum the partial tiles (chained: waits for the main grid)
