@@ -83,7 +83,9 @@ enum {
  * CUDA-core GEMV (where it applies: K % 32 == 0, r <= 256, M * (K + r) * 4
  * bytes <= 200 KiB; not in grouped calls); other calls run the tensor-core
  * kernels where they apply, else the CUDA-core GEMM.  GEMV selects the GEMV
- * for every forward of one or two tokens it applies to. */
+ * for every forward of one or two tokens it applies to.  The format-variant
+ * forwards (MXFP4 weights, FP32 adapters) have no GEMV: every selection but
+ * SIMT runs them on the tensor-core kernel where it applies. */
 enum { QERL_ALGO_AUTO = 0, QERL_ALGO_SIMT = 1, QERL_ALGO_TCGEN05 = 2, QERL_ALGO_GEMV = 3 };
 
 /*

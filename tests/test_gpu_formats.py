@@ -162,3 +162,38 @@ def test_f32_adapters_lora_term_precision(M, K, N, r, algo):
     bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * np.sqrt(np.mean(ref ** 2))
     assert (np.abs(got - ref) <= bound).all(), np.max(np.abs(got - ref) / bound)
     assert (got != ref_bf16).mean() < 0.02, (got != ref_bf16).mean()
+
+
+@pytest.mark.parametrize("chained", [True, False], ids=["chained", "serialised"])
+def test_variants_back_to_back_share_one_workspace(chained):
+    """Two MXFP4 forwards and two FP32-adapter forwards issued back to back on one
+    stream, each pair through one workspace, with no synchronisation between:
+    each call rewrites the workspace (the expanded scales, u) that the call before
+    it reads, so each output must still match its own oracle, with launches
+    chained (each kernel may start before its predecessor ends) and serialised."""
+    q.set_launch_chaining(chained)
+    try:
+        M, K, N, r = 8, 2048, 1024, 32
+        x = synth.activations(M, K, 100).cuda()
+        A = synth.lora_A(r, K, 101).cuda()
+        B = synth.lora_B(N, r, 102).cuda()
+        Ws = [synth.weight(N, K, 103 + i).cuda() * (2.0 ** (8 * i)) for i in range(2)]
+        mx = [q.qerl_mxfp4_quantize(W.to(torch.bfloat16)) for W in Ws]
+        ws = q.workspace(q.OP_MXFP4_FWD, M, N, K, r)
+        ys = [q.qerl_mxfp4_lora_linear_fwd(x, c, s, A, B, 2.0, ws=ws) for c, s in mx]
+        cases = [LinearCase(M, K, N, r, config=16, idx=i).quantize_gpu() for i in range(2)]
+        Af, Bf = _f32_adapters(r, K, N, 104)
+        wsf = q.workspace(q.OP_LINEAR_FWD_F32AB, M, N, K, r)
+        yf = [q.qerl_nvfp4_lora_linear_fwd_f32ab(c.x, c.codes, c.scales, c.ts, Af, Bf, 2.0, ws=wsf) for c in cases]
+        torch.cuda.synchronize()
+        assert q.get_error() == 0
+        for W, y in zip(Ws, ys):
+            rc, oc, osc = oracle.mxfp4_quantize(synth.bits(W.to(torch.bfloat16)))
+            ref = oracle.mxfp4_lora_linear_fwd(synth.bits(x), oc, osc, synth.bits(A), synth.bits(B), 2.0)
+            assert_rel_rms(f64(y), ref, LIN_TOL, "y (MXFP4)")
+        for c, y in zip(cases, yf):
+            oc, osc, ost = c.oracle_quant()
+            ref = oracle.lora_linear_fwd_f32ab(synth.bits(c.x), oc, osc, ost, Af.cpu().numpy(), Bf.cpu().numpy(), 2.0)
+            assert_rel_rms(f64(y), ref, LIN_TOL, "y (FP32 adapters)")
+    finally:
+        q.set_launch_chaining(True)
