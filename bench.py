@@ -777,7 +777,7 @@ def other_rows(dev, only=None, profile=False):
     # a4: Qwen2.5-14B prefill linears, M = 4096, r = 32
     wl = synth.WORKLOADS[2]
     M, tot_f, tot_s, per = 4096, 0.0, 0.0, {}
-    per_lin_args, per_lin_N, per_flops = {}, {}, {}
+    per_lin_args, per_lin_N, per_flops, w16_gu = {}, {}, {}, {}
     _, bf16, _, kind = peaks()
     if not want("a4"):
         wl = synth.Workload(wl.name, [], wl.M, wl.r, wl.hidden)
@@ -786,6 +786,8 @@ def other_rows(dev, only=None, profile=False):
         W = synth.weight(N, K, 20 + i, dev)
         c, sc, t = q.qerl_nvfp4_quantize(W)
         del W
+        if name in ("gate_proj", "up_proj") and want("a4"):  # the 16-bit arm of the grouped gate|up below
+            w16_gu[name] = q.qerl_nvfp4_dequantize(c, sc, t, N, K)
         q.qerl_nvfp4_pack_codes(c, out=c)
         A = synth.lora_A(wl.r, K, 40 + i, dev)
         B = synth.lora_B(N, wl.r, 60 + i, dev)
@@ -811,18 +813,51 @@ def other_rows(dev, only=None, profile=False):
         fl_g = sum(per_flops[n] for n in ("q_proj", "k_proj", "v_proj"))
         per["qkv_grouped"] = {"us": round(sec_g * 1e6, 1), "TFLOPs": round(fl_g / sec_g / 1e12, 1)}
         lay_s = sec_g + sum(per[n]["us"] for n in ("o_proj", "gate_proj", "up_proj", "down_proj")) / 1e6
+        # gate|up as one grouped call too (one pass over x for both down-projections,
+        # one launch of twice the tiles)
+        gu = [per_lin_args[n] for n in ("gate_proj", "up_proj")]
+        yu = [torch.empty(M, per_lin_N[n], dtype=torch.bfloat16, device=dev) for n in ("gate_proj", "up_proj")]
+        wsu = torch.empty(q.grouped_ws_bytes(M, per_lin_N["K_qkv"], wl.r, [per_lin_N[n] for n in ("gate_proj", "up_proj")]),
+                          dtype=torch.uint8, device=dev)
+        sec_u = timed(lambda: q.qerl_nvfp4_lora_linear_fwd_grouped(xq, gu, 2.0, packed=True, ys=yu, ws=wsu), 10)
+        fl_u = sum(per_flops[n] for n in ("gate_proj", "up_proj"))
+        # the same product in torch (cuBLAS bf16) on the dequantized weights of the same codes, concatenated:
+        # y_gate | y_up = x [W_gate; W_up]^T, plus each LoRA branch (x [A_gate; A_up]^T, then one small
+        # product per linear)
+        Ng, Nu = per_lin_N["gate_proj"], per_lin_N["up_proj"]
+        Wcat = torch.cat([w16_gu["gate_proj"], w16_gu["up_proj"]])
+        Acat = torch.cat([per_lin_args["gate_proj"][3], per_lin_args["up_proj"][3]])
+        Bg, Bu = per_lin_args["gate_proj"][4], per_lin_args["up_proj"][4]
+        ycat = torch.empty(M, Ng + Nu, dtype=torch.bfloat16, device=dev)
+        del w16_gu
+
+        def gate_up_bf16():
+            torch.mm(xq, Wcat.t(), out=ycat)
+            tcat = torch.mm(xq, Acat.t())
+            ycat[:, :Ng].add_(torch.mm(tcat[:, :wl.r], Bg.t()), alpha=2.0)
+            ycat[:, Ng:].add_(torch.mm(tcat[:, wl.r:], Bu.t()), alpha=2.0)
+        sec_b = timed(gate_up_bf16, 10)
+        per["gate_up_grouped"] = {"us": round(sec_u * 1e6, 1), "TFLOPs": round(fl_u / sec_u / 1e12, 1),
+                                  "bf16_cublas_us": round(sec_b * 1e6, 1),
+                                  "bf16_cublas_TFLOPs": round(fl_u / sec_b / 1e12, 1),
+                                  "speedup_vs_bf16": round(sec_b / sec_u, 3)}
+        del Wcat, ycat
+        lay_gg = sec_g + sec_u + sum(per[n]["us"] for n in ("o_proj", "down_proj")) / 1e6
         # the layer's two AQN-RMSNorms at M = 4096, H = 5120
         xn = synth.activations(M, wl.hidden, 15, dev)
         gn = synth.norm_gamma(wl.hidden, 16, dev)
         yn = torch.empty_like(xn)
         wsn = q.workspace(q.OP_AQN_RMSNORM, M, 0, wl.hidden, 0, dev)
         sec_n = timed(lambda: q.qerl_aqn_rmsnorm(xn, gn, 1e-6, 1e-2, 1, 5, 0, y=yn, ws=wsn), 20)
-        lay_n = lay_s + 2 * sec_n
+        lay_n = lay_gg + 2 * sec_n
         rows["a4_prefill"] = {"workload": wl.name, "TFLOPs": round(tot_f / tot_s / 1e12, 1),
                               "frac_of_bf16_peak": round(tot_f / tot_s / 1e12 / bf16, 3),
                               "layer_with_grouped_qkv_TFLOPs": round(tot_f / lay_s / 1e12, 1),
                               "layer_with_grouped_qkv_frac": round(tot_f / lay_s / 1e12 / bf16, 3),
+                              "layer_with_grouped_qkv_and_gate_up_TFLOPs": round(tot_f / lay_gg / 1e12, 1),
+                              "layer_with_grouped_qkv_and_gate_up_frac": round(tot_f / lay_gg / 1e12 / bf16, 3),
                               "layer_with_norms_us": round(lay_n * 1e6, 1),
+                              "layer_with_norms_is": "q|k|v and gate|up as grouped calls, o and down, two norms",
                               "layer_with_norms_TFLOPs": round(tot_f / lay_n / 1e12, 1),
                               "layer_with_norms_frac": round(tot_f / lay_n / 1e12 / bf16, 3),
                               "norm_us": round(sec_n * 1e6, 1),
