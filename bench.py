@@ -772,8 +772,15 @@ def other_rows(dev, only=None, profile=False):
         y = torch.empty_like(x)
         wsn = q.workspace(q.OP_AQN_RMSNORM, M, 0, H, 0, dev)
         sec = timed(lambda: q.qerl_aqn_rmsnorm(x, g, 1e-6, 1e-2, 1, 5, 0, y=y, ws=wsn), 50)
-        rows[f"a2_aqn_rmsnorm_{'decode' if M == 64 else 'prefill'}"] = {
-            "workload": tag, "us": round(sec * 1e6, 2), "GBps": round((4 * M * H + 6 * H) / sec / 1e9, 1)}
+        row = {"workload": tag, "us": round(sec * 1e6, 2), "GBps": round((4 * M * H + 6 * H) / sec / 1e9, 1)}
+        if M == 64:
+            # the same call 20 times in one CUDA graph (chained launches): the device time per call,
+            # without the host's per-call dispatch that paces the eager loop at this size
+            gr = _graph(lambda: [q.qerl_aqn_rmsnorm(x, g, 1e-6, 1e-2, 1, 5 + i, 0, y=y, ws=wsn) for i in range(20)])
+            _time_graph(gr, 3)
+            row["us_in_graph"] = round(_time_graph(gr, 10) / 200 * 1e6, 2)
+            del gr
+        rows[f"a2_aqn_rmsnorm_{'decode' if M == 64 else 'prefill'}"] = row
     # a4: Qwen2.5-14B prefill linears, M = 4096, r = 32
     wl = synth.WORKLOADS[2]
     M, tot_f, tot_s, per = 4096, 0.0, 0.0, {}
