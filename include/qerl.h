@@ -458,6 +458,21 @@ qerl_status qerl_decoder_chain_run(const qerl_chain *plan, float sigma, uint64_t
 /* Frees the host handle (the workspace stays the caller's). */
 void qerl_decoder_chain_destroy(qerl_chain *plan);
 
+/*
+ * Decoder-layer glue between the per-linear calls (the pages have no
+ * counterpart: these are the Qwen2.5 layer's residual add and SwiGLU, the
+ * operations the decoder chain fuses).  Elementwise over n bf16 values
+ * (device), each result rounded to bf16 once: out[i] = bf16(h[i] + y[i]), or
+ * bf16(silu(g[i]) * u[i]) with silu(g) = g / (1 + e^-g), computed in FP32 as
+ * g * sigmoid(g) from e^-|g| (no intermediate overflows).
+ * out may alias an input.  16-byte vector accesses when every pointer is
+ * 16-byte aligned and n % 8 == 0, else scalar ones.  Chained launches wait
+ * for the preceding work.  n = 0 launches nothing; NULL pointers or n < 0
+ * return QERL_ERR_INVALID_ARG.
+ */
+qerl_status qerl_residual_add(const void *h, const void *y, int64_t n, void *out, qerl_stream_t stream);
+qerl_status qerl_swiglu(const void *g, const void *u, int64_t n, void *out, qerl_stream_t stream);
+
 /* Scratch bytes an operation needs (0 if none).  Sizes as in the calls. */
 size_t qerl_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int r);
 

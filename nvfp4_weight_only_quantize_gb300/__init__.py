@@ -39,7 +39,7 @@ EXPORTED = ["qerl_nvfp4_quantize", "qerl_nvfp4_dequantize", "qerl_nvfp4_lora_lin
             "qerl_nvfp4_lora_linear_fwd_grouped",
             "qerl_launch_count", "qerl_decoder_chain_ws_bytes", "qerl_decoder_chain_plan",
             "qerl_decoder_chain_run", "qerl_decoder_chain_destroy", "qerl_mxfp4_quantize",
-            "qerl_mxfp4_lora_linear_fwd", "qerl_nvfp4_lora_linear_fwd_f32ab"]
+            "qerl_mxfp4_lora_linear_fwd", "qerl_nvfp4_lora_linear_fwd_f32ab", "qerl_residual_add", "qerl_swiglu"]
 
 
 class QerlError(RuntimeError):
@@ -104,6 +104,8 @@ def lib() -> C.CDLL:
             sig["qerl_decoder_chain_plan"] = ([vp, i32, vp, vp, vp, vp, sz, vp], i32)
             sig["qerl_decoder_chain_run"] = ([vp, f32, u64, u64, u32, vp], i32)
             sig["qerl_decoder_chain_destroy"] = ([vp], None)
+            sig["qerl_residual_add"] = ([vp, vp, i64, vp, vp], i32)
+            sig["qerl_swiglu"] = ([vp, vp, i64, vp, vp], i32)
             sig["qerl_nvfp4_lora_linear_fwd_packed"] = sig["qerl_nvfp4_lora_linear_fwd"]
             sig["qerl_nvfp4_lora_linear_bwd_packed"] = sig["qerl_nvfp4_lora_linear_bwd"]
             for name, (args, res) in sig.items():
@@ -339,6 +341,23 @@ def qerl_nvfp4_lora_linear_fwd_f32ab(x, codes, scales, tensor_scale, A, B, lora_
                                                   _stream(stream)),
            "qerl_nvfp4_lora_linear_fwd_f32ab")
     return y
+
+
+# ---------------------------------------------------------------- decoder-layer glue
+def qerl_residual_add(h, y, out=None, stream=None):
+    """out = bf16(h + y) elementwise (bf16 tensors of one shape); out may be h."""
+    assert h.shape == y.shape and h.dtype == y.dtype == torch.bfloat16
+    out = torch.empty_like(h) if out is None else out
+    _check(lib().qerl_residual_add(_p(h), _p(y), h.numel(), _p(out), _stream(stream)), "qerl_residual_add")
+    return out
+
+
+def qerl_swiglu(g, u, out=None, stream=None):
+    """out = bf16(silu(g) * u) elementwise (bf16 tensors of one shape)."""
+    assert g.shape == u.shape and g.dtype == u.dtype == torch.bfloat16
+    out = torch.empty_like(g) if out is None else out
+    _check(lib().qerl_swiglu(_p(g), _p(u), g.numel(), _p(out), _stream(stream)), "qerl_swiglu")
+    return out
 
 
 # ---------------------------------------------------------------- AQN

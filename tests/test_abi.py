@@ -66,6 +66,10 @@ def test_argument_errors_return_before_any_launch(L):
     assert L.qerl_aqn_noise(0, 0, 0, 0, fake, None, None) == 1
     assert L.qerl_set_linear_algo(9) == 1
     assert L.qerl_set_linear_algo(4) == 1
+    # decoder-layer glue: NULL pointers, negative length; an empty call launches nothing
+    assert L.qerl_residual_add(None, fake, 8, fake, None) == 1
+    assert L.qerl_swiglu(fake, fake, -1, fake, None) == 1
+    assert L.qerl_swiglu(fake, fake, 0, fake, None) == 0
     # format variants: K % 32 (MXFP4) / K % 16, r, missing or short workspace
     vargs = lambda K, r, wsp, wsb: (fake, 8, K, 16, fake, fake, fake, fake, r, 2.0, fake, None, wsp, wsb, None)
     assert L.qerl_mxfp4_lora_linear_fwd(*vargs(48, 4, ws, 1 << 20)) == 2
